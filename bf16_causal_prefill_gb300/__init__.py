@@ -1,0 +1,193 @@
+"""Causal prefill attention for NVIDIA GB300 (sm_103a): BF16 and per-block FP8.
+
+Python binding of the C-ABI library ``libzyfa.so`` (declared in
+``include/zyfa.h``). This module only marshals arguments: every step of the
+computation runs in the library's CUDA kernels. There is no CPU fallback; if
+the library is missing or the device is not sm_103, calls raise.
+
+Entry points (names follow the C ABI):
+  quantize_fp8(x, hadamard=False)            -> (codes uint8, scales float32)
+  attn_fwd_bf16(q, k, v, softmax_scale=None) -> o (bf16)
+  attn_fwd_fp8(q8, qs, k8, ks, v8, vs, ...)  -> o (bf16)
+  prefill_fp8(q, k, v, hadamard=False)       -> o: quantise Q, K, V then FP8 attention
+  device_status()                            -> raises ZyfaError on a kernel timeout
+
+Tensors are [B, S, H, D] with the head dimension contiguous.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "ZyfaError", "lib", "quantize_fp8", "attn_fwd_bf16", "attn_fwd_fp8", "prefill_fp8",
+    "device_status", "set_debug", "scale_blocks", "BLOCK_TOKENS",
+]
+
+BLOCK_TOKENS = 128
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG_DIR, "libzyfa.so")
+_lib = None
+
+_i64x3 = ctypes.c_int64 * 3
+
+
+class ZyfaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"zyfa error {code}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libzyfa.so (built by ``__graft_entry__.build()`` / ``_build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with bf16_causal_prefill_gb300._build.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, c_int, c_float = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    L.zyfa_status_string.restype = ctypes.c_char_p
+    L.zyfa_status_string.argtypes = [c_int]
+    L.zyfa_last_error_message.restype = ctypes.c_char_p
+    L.zyfa_last_error_message.argtypes = []
+    L.zyfa_version.restype = c_int
+    L.zyfa_quantize_fp8.restype = c_int
+    L.zyfa_quantize_fp8.argtypes = [vp, i64, i64, i64, vp, vp, c_int, c_int, c_int, c_int, c_int, vp]
+    L.zyfa_attn_fwd_bf16.restype = c_int
+    L.zyfa_attn_fwd_bf16.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                     vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_fp8.restype = c_int
+    L.zyfa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                                    c_float, vp, vp, vp, vp, vp]
+    L.zyfa_get_device_status.restype = c_int
+    L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    L.zyfa_set_debug.restype = c_int
+    L.zyfa_set_debug.argtypes = [c_int, ctypes.c_double]
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        L = lib()
+        raise ZyfaError(rc, L.zyfa_last_error_message().decode() or L.zyfa_status_string(rc).decode())
+
+
+def _stream_ptr(t: torch.Tensor, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return s.cuda_stream
+
+
+def _require(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be 4-D [B,S,H,D] with a contiguous last dim")
+
+
+def _strides(t: torch.Tensor):
+    return _i64x3(t.stride(0), t.stride(1), t.stride(2))
+
+
+def scale_blocks(S: int) -> int:
+    return (S + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+
+
+def quantize_fp8(x: torch.Tensor, hadamard: bool = False, out: Optional[torch.Tensor] = None,
+                 scales: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-(b, h, 128-token block) e4m3 quantisation of a bf16 [B,S,H,D] tensor.
+    Returns (codes uint8 [B,S,H,D] dense, scales float32 [B,H,ceil(S/128)])."""
+    _require(x, "x", torch.bfloat16)
+    B, S, H, D = x.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, scale_blocks(S)), dtype=torch.float32, device=x.device)
+    if not out.is_contiguous() or not scales.is_contiguous():
+        raise ValueError("out and scales must be contiguous")
+    _check(lib().zyfa_quantize_fp8(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), out.data_ptr(),
+                                   scales.data_ptr(), B, S, H, D, int(bool(hadamard)),
+                                   _stream_ptr(x, stream)))
+    return out, scales
+
+
+def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: Optional[float] = None,
+                  out: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Causal attention on bf16 q [B,S,Hq,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv] -> o [B,S,Hq,Dv] bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16)
+    B, S, Hq, Dqk = q.shape
+    Hkv, Dv = k.shape[2], v.shape[3]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    _require(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
+                                    Dqk, Dv, float(softmax_scale), _strides(q), _strides(k), _strides(v),
+                                    _strides(out), _stream_ptr(q, stream)))
+    return out
+
+
+def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor,
+                 v8: torch.Tensor, v_scale: torch.Tensor, softmax_scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Causal attention on per-block e4m3 inputs (uint8 codes + float32 block scales) -> bf16 o."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _require(t, n, torch.uint8)
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor")
+    B, S, Hq, Dqk = q8.shape
+    Hkv, Dv = k8.shape[2], v8.shape[3]
+    nb = scale_blocks(S)
+    if q_scale.shape != (B, Hq, nb) or k_scale.shape != (B, Hkv, nb) or v_scale.shape != (B, Hkv, nb):
+        raise ValueError("scale tensors must be [B, H, ceil(S/128)]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
+    _require(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                   v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk, Dv,
+                                   float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
+                                   _strides(out), _stream_ptr(q8, stream)))
+    return out
+
+
+def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
+                softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None):
+    """The FP8 prefill path: quantise Q and K (optionally rotated) and V, then
+    FP8 attention. Returns (o, (q8, qs, k8, ks, v8, vs))."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[3])
+    q8, qs = quantize_fp8(q, hadamard, stream=stream)
+    k8, ks = quantize_fp8(k, hadamard, stream=stream)
+    v8, vs = quantize_fp8(v, False, stream=stream)
+    o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream)
+    return o, (q8, qs, k8, ks, v8, vs)
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise and read/clear the device status word; raises on a timeout."""
+    w = ctypes.c_uint(0)
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check(lib().zyfa_get_device_status(s, ctypes.byref(w)))
+    return w.value
+
+
+def set_debug(stall_loader: bool = False, timeout_seconds: float = 0.0) -> None:
+    """Test hook: stall the attention loader warp and/or bound waits (seconds)."""
+    _check(lib().zyfa_set_debug(int(bool(stall_loader)), float(timeout_seconds)))

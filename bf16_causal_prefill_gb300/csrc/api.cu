@@ -1,0 +1,261 @@
+// C-ABI entry points: argument validation, TMA descriptor encoding, device
+// status word, and the launches of the quantiser and attention kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/zyfa.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(ZYFA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Per-device state, filled on first use of a device.
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* status = nullptr;   // address of the status word on this device
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+uint64_t g_timeout_ns = 2000000000ull;
+int g_debug_stall = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+}  // namespace
+
+// One word per device; kernels OR timeout codes into it.
+__device__ unsigned int zyfa_device_status_word;
+
+namespace {
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ZYFA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, zyfa_device_status_word)) != cudaSuccess)
+      return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+    d.status = static_cast<unsigned int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ZYFA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  if (!(d.cc_major == 10 && d.cc_minor == 3))
+    return fail(ZYFA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, d.cc_major,
+                d.cc_minor);
+  *out = &d;
+  return ZYFA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 4-D tiled map over a [B, S, H, D] tensor (dims innermost first: D, H, S, B),
+// box = 128 bytes of D x 1 head x 128 tokens x 1 batch, 128-byte swizzle,
+// out-of-range elements read as zero.
+int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elt, int D, int H, int S, int B,
+             const int64_t strides[3], const char* name) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(strides[2]) * elt,
+                                  static_cast<cuuint64_t>(strides[1]) * elt,
+                                  static_cast<cuuint64_t>(strides[0]) * elt};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), 1u, 128u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, gstrides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return ZYFA_OK;
+}
+
+int check_strides(const int64_t s[3], int64_t mult, const char* name) {
+  if (!s) return fail(ZYFA_ERR_INVALID_ARG, "%s strides pointer is null", name);
+  for (int i = 0; i < 3; ++i) {
+    if (s[i] <= 0) return fail(ZYFA_ERR_INVALID_ARG, "%s stride[%d] = %lld must be positive", name, i, (long long)s[i]);
+    if (s[i] % mult != 0)
+      return fail(ZYFA_ERR_INVALID_ARG, "%s stride[%d] = %lld must be a multiple of %lld elements", name, i,
+                  (long long)s[i], (long long)mult);
+    if (s[i] >= (int64_t(1) << 38)) return fail(ZYFA_ERR_INVALID_ARG, "%s stride[%d] too large", name, i);
+  }
+  return ZYFA_OK;
+}
+
+struct AttnCommon {
+  int B, S, Hq, Hkv, Dqk, Dv;
+  float softmax_scale;
+};
+
+int validate_attn(const AttnCommon& c, const void* q, const void* k, const void* v, void* o, int64_t in_mult,
+                  const int64_t qs[3], const int64_t ks[3], const int64_t vs[3], const int64_t os[3]) {
+  if (!q || !k || !v || !o) return fail(ZYFA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ZYFA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (c.B < 1 || c.S < 1 || c.Hq < 1 || c.Hkv < 1)
+    return fail(ZYFA_ERR_INVALID_ARG, "B, S, Hq, Hkv must be >= 1 (got %d, %d, %d, %d)", c.B, c.S, c.Hq, c.Hkv);
+  if (c.Hq % c.Hkv != 0) return fail(ZYFA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", c.Hq, c.Hkv);
+  if (!((c.Dqk == 128 && c.Dv == 128) || (c.Dqk == 192 && c.Dv == 128)))
+    return fail(ZYFA_ERR_UNSUPPORTED, "head dims (%d, %d) unsupported; use (128, 128) or (192, 128)", c.Dqk, c.Dv);
+  if (!(c.softmax_scale > 0.f) || !std::isfinite(c.softmax_scale))
+    return fail(ZYFA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  const long long n_qtiles = (c.S + 127) / 128;
+  if (static_cast<long long>(c.B) * c.Hq * ((n_qtiles + 1) / 2) >= (1LL << 31))
+    return fail(ZYFA_ERR_INVALID_ARG, "problem too large");
+  int r;
+  if ((r = check_strides(qs, in_mult, "q")) || (r = check_strides(ks, in_mult, "k")) ||
+      (r = check_strides(vs, in_mult, "v")) || (r = check_strides(os, 8, "o")))
+    return r;
+  return ZYFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int zyfa_version(void) { return 100; }
+
+const char* zyfa_status_string(int status) {
+  switch (status) {
+    case ZYFA_OK: return "ok";
+    case ZYFA_ERR_INVALID_ARG: return "invalid argument";
+    case ZYFA_ERR_UNSUPPORTED: return "unsupported";
+    case ZYFA_ERR_CUDA: return "CUDA error";
+    case ZYFA_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* zyfa_last_error_message(void) { return g_last_error; }
+
+int zyfa_set_debug(int stall_loader, double timeout_seconds) {
+  g_debug_stall = stall_loader ? 1 : 0;
+  g_timeout_ns = timeout_seconds > 0 ? static_cast<uint64_t>(timeout_seconds * 1e9) : 2000000000ull;
+  return ZYFA_OK;
+}
+
+int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                      float* scales, int B, int S, int H, int D, int hadamard, void* stream) {
+  if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
+  if (B < 1 || S < 1 || H < 1) return fail(ZYFA_ERR_INVALID_ARG, "B, S, H must be >= 1");
+  if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
+  if (hadamard && D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
+  if (!aligned(x, 4) || !aligned(out, 2) || !aligned(scales, 4))
+    return fail(ZYFA_ERR_INVALID_ARG, "misaligned pointer");
+  if (stride_b <= 0 || stride_s <= 0 || stride_h <= 0 || (stride_b | stride_s | stride_h) & 1)
+    return fail(ZYFA_ERR_INVALID_ARG, "strides must be positive and even");
+  if ((static_cast<long long>(S) + 127) / 128 > 65535 * 1024LL || H > 65535 || B > 65535)
+    return fail(ZYFA_ERR_INVALID_ARG, "grid too large");
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  zyfa::QuantArgs a{x, stride_b, stride_s, stride_h, static_cast<uint8_t*>(out), scales, B, S, H, D, hadamard};
+  cudaError_t e = zyfa::launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8 launch");
+  return ZYFA_OK;
+}
+
+static int attn_common(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
+                       const float* vsc, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
+                       float softmax_scale, const int64_t qs[3], const int64_t ks[3], const int64_t vs[3],
+                       const int64_t os[3], void* stream) {
+  AttnCommon c{B, S, Hq, Hkv, Dqk, Dv, softmax_scale};
+  const int elt = fp8 ? 1 : 2;
+  if (int r = validate_attn(c, q, k, v, o, 16 / elt, qs, ks, vs, os)) return r;
+  if (fp8) {
+    if (!qsc || !ksc || !vsc) return fail(ZYFA_ERR_INVALID_ARG, "null scale pointer");
+    if (!aligned(qsc, 4) || !aligned(ksc, 4) || !aligned(vsc, 4))
+      return fail(ZYFA_ERR_INVALID_ARG, "scale pointers must be 4-byte aligned");
+  }
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tq, tk, tv;
+  int r;
+  if ((r = make_map(&tq, q, dt, elt, Dqk, Hq, S, B, qs, "q")) || (r = make_map(&tk, k, dt, elt, Dqk, Hkv, S, B, ks, "k")) ||
+      (r = make_map(&tv, v, dt, elt, Dv, Hkv, S, B, vs, "v")))
+    return r;
+  zyfa::AttnArgs a;
+  a.B = B; a.S = S; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o; a.o_sb = os[0]; a.o_ss = os[1]; a.o_sh = os[2];
+  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.debug_stall = g_debug_stall;
+  a.num_sms = d->sm_count;
+  cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
+                      : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
+  return ZYFA_OK;
+}
+
+int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                       int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                       const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
+  return attn_common(false, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
+                     k_strides, v_strides, o_strides, stream);
+}
+
+int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale, const void* v8,
+                      const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
+                      float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                      const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
+  return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream);
+}
+
+int zyfa_get_device_status(void* stream, unsigned int* word) {
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  unsigned int w = 0;
+  if ((e = cudaMemcpyFromSymbol(&w, zyfa_device_status_word, sizeof(w))) != cudaSuccess)
+    return fail_cuda(e, "read status word");
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpyToSymbol(zyfa_device_status_word, &zero, sizeof(zero))) != cudaSuccess)
+    return fail_cuda(e, "clear status word");
+  if (word) *word = w;
+  if (w) return fail(ZYFA_ERR_TIMEOUT, "device status word 0x%x: a kernel wait timed out", w);
+  return ZYFA_OK;
+}
+
+}  // extern "C"

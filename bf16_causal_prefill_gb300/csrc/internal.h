@@ -1,0 +1,46 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not installed; callers use include/zyfa.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace zyfa {
+
+constexpr int kBlockTokens = 128;   // quantisation block and attention tile height
+constexpr int kTileKeys = 128;      // keys per K/V tile
+
+struct QuantArgs {
+  const void* x;          // bf16 [B,S,H,D], element strides sb, ss, sh; last dim contiguous
+  int64_t sb, ss, sh;
+  uint8_t* out;           // e4m3 [B,S,H,D] dense
+  float* scales;          // [B,H,ceil(S/128)]
+  int B, S, H, D;
+  int hadamard;
+};
+
+cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  int B, S, Hq, Hkv, Dqk, Dv;
+  float scale_log2;        // softmax_scale * log2(e)
+  void* o;                 // bf16 [B,S,Hq,Dv]
+  int64_t o_sb, o_ss, o_sh;
+  const float* q_scale;    // fp8 only: [B,Hq,nblk]
+  const float* k_scale;    // fp8 only: [B,Hkv,nblk]
+  const float* v_scale;    // fp8 only: [B,Hkv,nblk]
+  unsigned int* status;    // device status word
+  uint64_t timeout_ns;     // bound on every barrier wait
+  int debug_stall;         // nonzero: the loader issues nothing (watchdog test)
+  int num_sms;
+};
+
+// tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of
+// 128 bytes x 1 head x 128 tokens x 1 batch.
+cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                            const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace zyfa

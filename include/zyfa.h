@@ -1,0 +1,151 @@
+/*
+ * zyfa.h -- C ABI of the GB300 causal prefill attention library.
+ *
+ * One computation: causal forward (prefill) attention in BF16 and FP8 e4m3,
+ * head dim 128 (with grouped-query heads) and the MLA head shape (query-key
+ * dim 192, value dim 128), with per-block FP8 scaling of Q, K, V and of the
+ * probabilities, normalisation by the rounded row sum, and an optional
+ * 128-point Hadamard rotation of Q and K before quantisation.
+ *
+ * Sources of the operations (page title, section):
+ *   - "ZYFA: Fast and Accurate FP8 Attention on AMD MI355X": "Introduction"
+ *     and "Methodology and Limitations" (causal forward pass, equal query and
+ *     key lengths, head dim 128 and the MLA shape); "Per-Block Scaling and
+ *     Normalization by the Rounded Row Sum"; "FP8 Error in Full-Model
+ *     Inference" and footnote 2 (Hadamard rotation fused into the Q pass).
+ *   - "FP8 GEMM on CDNA4": section 2.1 (e4m3, max 448), 2.2 (scale = amax /
+ *     max, guard for all-zero blocks), 2.3 (round to nearest even).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are [B, S, H, D] with the last (head) dimension contiguous.
+ *     Strides are in ELEMENTS for the batch, sequence and head dimensions.
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference to them after the call returns and allocates no
+ *     device memory on the caller's behalf.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
+ *     enqueued asynchronously; nothing synchronises unless stated.
+ *   - Arguments are validated on the host before anything is launched; on
+ *     a validation error nothing is enqueued. The text of the last error of
+ *     the calling thread is available from zyfa_last_error_message().
+ *   - Kernels are built for sm_103a only; another device returns
+ *     ZYFA_ERR_UNSUPPORTED.
+ *   - Every wait inside the kernels is bounded. A kernel that times out
+ *     writes a code into a per-device status word and exits cleanly; read it
+ *     with zyfa_get_device_status().
+ */
+#ifndef ZYFA_H_
+#define ZYFA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZYFA_OK = 0,
+  ZYFA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or stride */
+  ZYFA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  ZYFA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  ZYFA_ERR_TIMEOUT = 4       /* a kernel's bounded wait expired (device status) */
+} zyfa_status;
+
+/* Static text for a status code. */
+const char* zyfa_status_string(int status);
+
+/* Thread-local description of the last non-OK return on this thread. */
+const char* zyfa_last_error_message(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int zyfa_version(void);
+
+/*
+ * Per-block FP8 quantisation ("FP8 GEMM on CDNA4" 2.2-2.3; rotation: ZYFA
+ * post, "FP8 Error in Full-Model Inference").
+ *
+ * For every (b, h, 128-token block j) over the whole head dimension:
+ *   y     = hadamard ? FWHT_128(x) * fl32(1/sqrt(128)) : x        (fp32)
+ *   amax  = max |y|;  scale = (amax < 1e-8f) ? 1 : RN(amax / 448)
+ *   out   = e4m3 code of RN(y / scale), round to nearest even, saturating
+ *           at +-448, sign kept for results that round to zero
+ *   scales[(b*H + h)*ceil(S/128) + j] = scale
+ * The FWHT runs butterflies of span 1, 2, ..., 64 in that order, each rounded
+ * to fp32; results are bit-exact and deterministic.
+ *
+ * x      : bf16 [B,S,H,D], strides (stride_b, stride_s, stride_h) elements,
+ *          4-byte aligned, stride_* even.
+ * out    : uint8 e4m3 codes [B,S,H,D], dense (row-major), caller-allocated.
+ * scales : float [B,H,ceil(S/128)], dense, caller-allocated.
+ * D      : 128 or 192. hadamard (0/1) requires D == 128.
+ * Errors : ZYFA_ERR_INVALID_ARG (null/misaligned pointer, B/S/H < 1, odd
+ *          stride), ZYFA_ERR_UNSUPPORTED (other D, hadamard with D != 128,
+ *          device not sm_103), ZYFA_ERR_CUDA (launch failure).
+ */
+int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                      float* scales, int B, int S, int H, int D, int hadamard, void* stream);
+
+/*
+ * Causal attention, BF16 in and out ("ZYFA ..." Introduction; grouped-query
+ * heads: query head h reads KV head h / (Hq / Hkv)):
+ *   O[b,i,h,:] = sum_{j<=i} softmax_j(softmax_scale * Q[b,i,h].K[b,j,g]) V[b,j,g]
+ * Probabilities are rounded to bf16 for the PV product; the row sum uses the
+ * unrounded fp32 probabilities; accumulation is fp32; output rounded to bf16.
+ *
+ * q : bf16 [B,S,Hq,Dqk]; k : bf16 [B,S,Hkv,Dqk]; v : bf16 [B,S,Hkv,Dv];
+ * o : bf16 [B,S,Hq,Dv], caller-allocated, must not alias q/k/v.
+ * *_strides[3] : (batch, seq, head) strides in elements. q/k/v strides must
+ *          be multiples of 8 elements (16 bytes, TMA); o strides multiples of
+ *          8 elements. All pointers 16-byte aligned.
+ * (Dqk, Dv) : (128, 128) or (192, 128). Hq % Hkv == 0. S >= 1 (any length;
+ *          the last tile is masked). softmax_scale > 0 and finite.
+ * Errors : ZYFA_ERR_INVALID_ARG, ZYFA_ERR_UNSUPPORTED, ZYFA_ERR_CUDA.
+ */
+int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                       int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
+                       const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
+                       void* stream);
+
+/*
+ * Causal attention on per-block FP8 inputs ("ZYFA ...", "Per-Block Scaling
+ * and Normalization by the Rounded Row Sum"). Inputs are e4m3 codes with one
+ * fp32 scale per (b, h, 128-token block), as written by zyfa_quantize_fp8;
+ * the dequantised value is code * scale. Within each 128-key tile the
+ * probabilities of a row are multiplied by a power of two that puts their
+ * maximum in (0.5, 1], rounded to e4m3 (RNE), multiplied by V on the tensor
+ * cores with fp32 accumulation, and each row is divided by the sum of the
+ * rounded probabilities (the power of two divided back out), so the weights
+ * that multiply V sum to one. Output bf16.
+ *
+ * q8/k8/v8 : uint8 e4m3 [B,S,H,D] with the given strides (multiples of 16
+ *            elements), 16-byte aligned.
+ * q_scale  : float [B,Hq,ceil(S/128)], k_scale/v_scale: float [B,Hkv,ceil(S/128)].
+ * Other arguments and errors as zyfa_attn_fwd_bf16.
+ */
+int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                      const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                      int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                      const int64_t v_strides[3], const int64_t o_strides[3], void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. *word receives the raw bits (0 when every kernel finished normally;
+ * bit 0: loader wait timed out, bit 1: MMA wait, bit 2: softmax wait,
+ * bit 8: drain after abort incomplete). Returns ZYFA_ERR_TIMEOUT if any bit
+ * was set, ZYFA_ERR_CUDA if the synchronisation failed, else ZYFA_OK.
+ * `word` may be NULL.
+ */
+int zyfa_get_device_status(void* stream, unsigned int* word);
+
+/*
+ * Test hooks (process-wide, not thread-safe). stall_loader != 0 makes the
+ * attention kernels' loader warp issue nothing, so every consumer wait runs
+ * out; timeout_seconds bounds each wait (default 2.0; <= 0 restores it).
+ * Used to test the watchdog path without faulting the GPU.
+ */
+int zyfa_set_debug(int stall_loader, double timeout_seconds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZYFA_H_ */

@@ -63,10 +63,20 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
     return np.where(codes & 0x80, -mag, mag)
 
 
-def e4m3_rne(q: np.ndarray) -> np.ndarray:
+def e4m3_rne(q: np.ndarray, chunk: int = 1 << 22) -> np.ndarray:
     """Round float values to e4m3 codes: nearest code, ties to even mantissa,
     saturating at 448, sign kept (a negative value that rounds to zero gives
-    0x80). The nearest code is found by searching the full table of codes."""
+    0x80). The nearest code is found by searching the full table of codes.
+    Large arrays are processed in chunks of `chunk` elements."""
+    q = np.asarray(q)
+    flat = q.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    for s in range(0, flat.size, chunk):
+        out[s:s + chunk] = _e4m3_rne_flat(flat[s:s + chunk])
+    return out.reshape(q.shape)
+
+
+def _e4m3_rne_flat(q: np.ndarray) -> np.ndarray:
     q = np.asarray(q, dtype=np.float64)
     a = np.abs(q)
     idx = np.searchsorted(E4M3_VALUES, a, side="left")      # first value >= a
@@ -105,26 +115,23 @@ def quantize_fp8(x: np.ndarray, hadamard: bool = False, block: int = BLOCK_TOKEN
 
     x: [B, S, H, D] values exactly representable in float32 (the bf16 input).
     Returns (codes uint8 [B, S, H, D], scales float32 [B, H, ceil(S/block)]).
+    Each (b, h, token block) is reduced on its own; a ragged last block uses
+    only its own rows (the zero padding below cannot raise |y|'s maximum).
     """
     x = np.asarray(x, dtype=np.float32)
     B, S, H, D = x.shape
     y = fwht128_fp32(x) if hadamard else x
     nblk = (S + block - 1) // block
-    codes = np.empty((B, S, H, D), dtype=np.uint8)
-    scales = np.empty((B, H, nblk), dtype=np.float32)
-    for b in range(B):
-        for h in range(H):
-            for j in range(nblk):
-                yb = y[b, j * block:(j + 1) * block, h, :]
-                amax = np.float32(np.max(np.abs(yb)))
-                if amax < ZERO_GUARD:
-                    scale = np.float32(1.0)
-                else:
-                    scale = np.float32(amax / np.float32(E4M3_MAX))
-                q = (yb / scale).astype(np.float32)
-                codes[b, j * block:(j + 1) * block, h, :] = e4m3_rne(q)
-                scales[b, h, j] = scale
-    return codes, scales
+    pad = nblk * block - S
+    if pad:
+        y = np.concatenate([y, np.zeros((B, pad, H, D), np.float32)], axis=1)
+    yb = y.reshape(B, nblk, block, H, D)
+    amax = np.abs(yb).max(axis=(2, 4))                                   # [B, nblk, H], float32
+    scale = np.where(amax < ZERO_GUARD, np.float32(1.0),
+                     (amax / np.float32(E4M3_MAX)).astype(np.float32)).astype(np.float32)
+    q = (yb / scale[:, :, None, :, None]).astype(np.float32)              # IEEE float32 division
+    codes = e4m3_rne(q).reshape(B, nblk * block, H, D)[:, :S]
+    return np.ascontiguousarray(codes), np.ascontiguousarray(scale.transpose(0, 2, 1))
 
 
 def dequantize_fp8(codes: np.ndarray, scales: np.ndarray, block: int = BLOCK_TOKENS):

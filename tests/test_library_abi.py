@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol that
+include/zyfa.h declares, and rejects bad arguments on the host before any
+launch (these calls never reach a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import bf16_causal_prefill_gb300 as zyfa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zyfa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return zyfa.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zyfa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("zyfa_quantize_fp8", "zyfa_attn_fwd_bf16", "zyfa_attn_fwd_fp8", "zyfa_get_device_status",
+              "zyfa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), f"libzyfa.so does not export {n}"
+
+
+def test_status_strings(L):
+    assert L.zyfa_status_string(0) == b"ok"
+    assert L.zyfa_status_string(4) == b"kernel wait timed out"
+    assert L.zyfa_version() >= 100
+
+
+I3 = ctypes.c_int64 * 3
+
+
+def _bf16(L, **kw):
+    a = dict(q=16, k=16, v=16, o=16, B=1, S=128, Hq=2, Hkv=1, Dqk=128, Dv=128, scale=0.1,
+             qs=I3(256, 256, 128), ks=I3(128, 128, 128), vs=I3(128, 128, 128), os_=I3(256, 256, 128))
+    a.update(kw)
+    return L.zyfa_attn_fwd_bf16(a["q"], a["k"], a["v"], a["o"], a["B"], a["S"], a["Hq"], a["Hkv"], a["Dqk"],
+                                a["Dv"], ctypes.c_float(a["scale"]), a["qs"], a["ks"], a["vs"], a["os_"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1),                      # null pointer
+    (dict(k=8), 1),                      # misaligned pointer
+    (dict(Hq=3, Hkv=2), 1),              # Hq not a multiple of Hkv
+    (dict(S=0), 1),
+    (dict(Dqk=64, Dv=64), 2),            # unsupported head dims
+    (dict(Dqk=192, Dv=192), 2),
+    (dict(scale=-1.0), 1),
+    (dict(qs=I3(256, 256, 100)), 1),     # stride not 16-byte multiple
+    (dict(os_=I3(256, 0, 128)), 1),
+])
+def test_attention_rejects_bad_arguments_on_host(L, kw, code):
+    assert _bf16(L, **kw) == code
+    assert L.zyfa_last_error_message()
+
+
+def test_quantiser_rejects_bad_arguments_on_host(L):
+    q = L.zyfa_quantize_fp8
+    assert q(None, 1, 1, 1, 16, 16, 1, 1, 1, 128, 0, None) == 1
+    assert q(16, 64, 64, 64, 16, 16, 1, 1, 1, 64, 0, None) == 2          # D
+    assert q(16, 192, 192, 192, 16, 16, 1, 1, 1, 192, 1, None) == 2       # rotation needs D=128
+    assert q(16, 3, 128, 128, 16, 16, 1, 1, 1, 128, 0, None) == 1          # odd stride
+
+
+def test_fp8_attention_needs_scales(L):
+    rc = L.zyfa_attn_fwd_fp8(16, None, 16, 16, 16, 16, 16, 1, 128, 2, 1, 128, 128, ctypes.c_float(0.1),
+                             I3(256, 256, 128), I3(128, 128, 128), I3(128, 128, 128), I3(256, 256, 128), None)
+    assert rc == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 128, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        zyfa.quantize_fp8(x)
