@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark: causal prefill attention TFLOP/s at 32K tokens on GB300.
+
+Workload (default): batch 1, 32 query heads / 8 KV heads, 32768 tokens, head
+dim 128, Gaussian N(0,1) Q/K/V drawn in bf16 from seed 0 (``workloads``).
+One step is one pass of the whole hot path over that input:
+  * FP8 path (the headline ``value``): quantise Q, K, V per 128-token block
+    (3 launches of the quantiser) and run FP8 causal attention (1 launch);
+  * BF16 path (reported under ``bf16``): BF16 causal attention (1 launch).
+TFLOP/s counts causal FLOPs B*Hq*S^2*(Dqk+Dv) per step.
+
+Timing: W untimed warm-up steps, then exactly K steps; each step bracketed by
+CUDA events on the launching stream, with a 256 MiB L2 flush between steps
+(outside the events; the inputs are larger than L2 as well). Barrier and
+device synchronisation on both sides; the time is the max over ranks. Under
+torchrun every rank runs its own replica of the workload on its own GPU
+(replicas only: the path has no exchange step), and ``value`` counts the
+work of all ranks.
+
+``--impl reference`` times the CPU oracle (float64 attention and the fp32
+quantiser emulation) on a bounded sample of the same workload; only rank 0
+runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal prefill attn TFLOP/s (FP8, BF16) at 32K tokens; % of GB300 dense peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor-core rate ratio on GB300
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["zyfa", "reference"], default="zyfa")
+    p.add_argument("--workload", default=None, help="workload name (default: the 32K GQA shape)")
+    p.add_argument("--hadamard", action="store_true", help="rotate Q and K before quantisation")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- peaks --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_from_profiles(kernel_file: str, tag: str):
+    """Per-launch DRAM bytes recorded in profiles/ for `tag`, if the kernel
+    source still has the hash the counters were taken with; else None."""
+    src = os.path.join(ROOT, "bf16_causal_prefill_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    pat = re.compile(rf"^traffic\[{re.escape(tag)}\]:\s*([0-9.eE+]+)\s+bytes/launch\s+src=([0-9a-f]+)")
+    pdir = os.path.join(ROOT, "profiles")
+    for name in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m and m.group(2) == h:
+                    return float(m.group(1))
+    return None
+
+
+# -------------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                     util=float(parts[4]), hw=parts[6], hwt=parts[7], swt=parts[8],
+                                     swpc=parts[9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swpc", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in loaded),
+                "power_w_max": max(r["power"] for r in loaded), "samples": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+def clocks_rejected(c) -> bool:
+    if not c:
+        return False
+    if set(c["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}:
+        return True
+    return c["sm_mhz"] < 0.5 * c["sm_max_mhz"] and not c["reasons"]
+
+
+# ---------------------------------------------------------- CPU oracle timing --
+class OracleSampler:
+    """Times the oracle's FP8 path on a sample of the workload: the first
+    min(S, 4096) tokens are quantised once (fp32 quantiser emulation), then
+    each call computes random (batch, head, row) outputs in float64 for a
+    time budget. Per-element and per-FLOP times extrapolate to the full
+    workload."""
+
+    def __init__(self, workload_name: str, hadamard: bool):
+        import numpy as np
+        import workloads
+        from oracle import fp8 as ofp8
+
+        self.w = w = workloads.get(workload_name)
+        self.s_lim = min(w.S, 4096)
+        q, k, v = workloads.make_qkv(w.with_seq(self.s_lim, name=w.name))
+        q32, k32, v32 = q.float().numpy(), k.float().numpy(), v.float().numpy()
+        had = hadamard and w.Dqk == 128
+        t0 = time.perf_counter()
+        cq, sq = ofp8.quantize_fp8(q32, had)
+        ck, sk = ofp8.quantize_fp8(k32, had)
+        cv, sv = ofp8.quantize_fp8(v32, False)
+        self.qd, self.kd, self.vd = (ofp8.dequantize_fp8(cq, sq), ofp8.dequantize_fp8(ck, sk),
+                                     ofp8.dequantize_fp8(cv, sv))
+        self.t_quant = time.perf_counter() - t0
+        self.elems = q32.size + k32.size + v32.size
+        self.rng = np.random.default_rng(0)
+
+    def step(self, budget_s: float):
+        from oracle import attention as oattn
+        w = self.w
+        flops, rows = 0.0, 0
+        t1 = time.perf_counter()
+        while time.perf_counter() - t1 < budget_s or rows == 0:
+            b = int(self.rng.integers(0, w.B))
+            h = int(self.rng.integers(0, w.Hq))
+            i = int(self.rng.integers(0, self.s_lim))
+            oattn.causal_attention_rows(self.qd, self.kd, self.vd, w.softmax_scale, b, h, [i])
+            flops += 2.0 * (i + 1) * (w.Dqk + w.Dv)
+            rows += 1
+        t_attn = time.perf_counter() - t1
+        full_elems = w.B * w.S * (w.Hq * w.Dqk + w.Hkv * (w.Dqk + w.Dv))
+        t_full = self.t_quant / self.elems * full_elems + t_attn / flops * w.causal_flops
+        return {"value": w.causal_flops / t_full / 1e12, "t_full_s": t_full, "rows": rows,
+                "sample": (f"oracle FP8 path (fp32 quantiser emulation, dequantise, float64 attention) on the "
+                           f"first {self.s_lim} tokens: Q/K/V quantised once ({self.t_quant:.1f} s), then "
+                           f"{rows} random (batch, head, row) outputs ({t_attn:.1f} s); per-element and "
+                           f"per-FLOP times extrapolated to the full workload ({t_full:.0f} s)")}
+
+
+def _pin_cpu_threads():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+
+
+def run_cpu_worker(spec: str):
+    d = json.loads(spec)
+    res = OracleSampler(d["workload"], d["hadamard"]).step(d["budget_s"])
+    print("CPU_WORKER_RESULT " + json.dumps(res))
+
+
+def cpu_baseline(workload_name: str, budget_s: float, hadamard: bool):
+    """Run the oracle sample in a fresh single-threaded process."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    spec = json.dumps({"workload": workload_name, "budget_s": budget_s, "hadamard": hadamard})
+    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec], env=env,
+                       capture_output=True, text=True, timeout=900)
+    for line in p.stdout.splitlines():
+        if line.startswith("CPU_WORKER_RESULT "):
+            res = json.loads(line[len("CPU_WORKER_RESULT "):])
+            res.update({"unit": UNIT, "cores": 1, "kind": "oracle"})
+            return res
+    raise RuntimeError(f"cpu baseline worker failed:\n{p.stdout[-2000:]}\n{p.stderr[-2000:]}")
+
+
+# ---------------------------------------------------------------- distributed --
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------- main --
+def main_reference(args):
+    _pin_cpu_threads()
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import workloads
+    name = args.workload or workloads.BENCH
+    w = workloads.get(name)
+    K, W = args.steps, max(args.warmup, 3)
+    per_step = max(0.3, min(6.0, 150.0 / (K + W)))
+    sampler = OracleSampler(name, args.hadamard)
+    for _ in range(W):
+        sampler.step(per_step * 0.2)
+    t_full = []
+    last = None
+    for _ in range(K):
+        last = sampler.step(per_step)
+        t_full.append(last["t_full_s"])
+    t_mean = statistics.mean(t_full)
+    value = w.causal_flops / t_mean / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": t_mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3 path emulated (fp32 quantiser, float64 attention)",
+        "data": "synthetic (seeded Gaussian, bf16)",
+        "config": {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "Dqk": w.Dqk, "Dv": w.Dv,
+                   "path": "oracle: quantise Q/K/V + attention", "hadamard": bool(args.hadamard)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "each step: " + last["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.cpu_worker:
+        run_cpu_worker(args.cpu_worker)
+        return
+    if args.impl == "reference":
+        main_reference(args)
+        return
+
+    import torch
+    import __graft_entry__
+    import bf16_causal_prefill_gb300 as zyfa
+    import workloads
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    zyfa.lib()
+    dev = torch.device("cuda", local)
+    name = args.workload or workloads.BENCH
+    w = workloads.get(name)
+    K, W = args.steps, max(args.warmup, 3)
+    had = bool(args.hadamard) and w.Dqk == 128
+
+    q, k, v = workloads.make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    nb = zyfa.scale_blocks(w.S)
+    q8 = torch.empty(qd.shape, dtype=torch.uint8, device=dev)
+    k8 = torch.empty(kd.shape, dtype=torch.uint8, device=dev)
+    v8 = torch.empty(vd.shape, dtype=torch.uint8, device=dev)
+    qs = torch.empty((w.B, w.Hq, nb), dtype=torch.float32, device=dev)
+    ks = torch.empty((w.B, w.Hkv, nb), dtype=torch.float32, device=dev)
+    vs = torch.empty((w.B, w.Hkv, nb), dtype=torch.float32, device=dev)
+    o8 = torch.empty((w.B, w.S, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    o16 = torch.empty_like(o8)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fp8_step(ev_attn=None):
+        zyfa.quantize_fp8(qd, had, out=q8, scales=qs)
+        zyfa.quantize_fp8(kd, had, out=k8, scales=ks)
+        zyfa.quantize_fp8(vd, False, out=v8, scales=vs)
+        if ev_attn is not None:
+            ev_attn[0].record(stream)
+        zyfa.attn_fwd_fp8(q8, qs, k8, ks, v8, vs, w.softmax_scale, out=o8)
+        if ev_attn is not None:
+            ev_attn[1].record(stream)
+
+    def bf16_step(ev_attn=None):
+        if ev_attn is not None:
+            ev_attn[0].record(stream)
+        zyfa.attn_fwd_bf16(qd, kd, vd, w.softmax_scale, out=o16)
+        if ev_attn is not None:
+            ev_attn[1].record(stream)
+
+    def timed(step, n_steps, n_warm):
+        for _ in range(n_warm):
+            step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+        ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(n_steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(ev_k[i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        t_step = sum(a.elapsed_time(b) for a, b in ev) / n_steps          # ms
+        t_kern = sum(a.elapsed_time(b) for a, b in ev_k) / n_steps        # ms
+        zyfa.device_status()
+        return t_step, t_kern
+
+    sampler = ClockSampler(local)
+    for attempt in range(2):
+        sampler.start()
+        t8, t8k = timed(fp8_step, K, W)
+        t16, t16k = timed(bf16_step, K, W)
+        clocks = sampler.stop()
+        if not clocks_rejected(clocks):
+            break
+    t8 = max_over_ranks(t8, world)
+    t16 = max_over_ranks(t16, world)
+
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(o8.shape, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step(ev_attn=None):
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            fp8_step(ev_attn)
+            ho.copy_(o8, non_blocking=True)
+
+        te, _ = timed(e2e_step, max(3, min(K, 20)), 3)
+        te = max_over_ranks(te, world)
+        e2e = {"value": world * w.causal_flops / (te * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (q, k, v))),
+               "d2h_bytes_per_step": int(o8.numel() * o8.element_size()), "ms_per_step": te,
+               "path": "pinned host bf16 Q/K/V -> device, quantise + FP8 attention, bf16 O -> pinned host"}
+
+    peaks, src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8_peak_sus = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    v8 = world * w.causal_flops / (t8 * 1e-3) / 1e12
+    v16 = world * w.causal_flops / (t16 * 1e-3) / 1e12
+    a8 = w.causal_flops / (t8k * 1e-3) / 1e12
+    a16 = w.causal_flops / (t16k * 1e-3) / 1e12
+    tr8 = traffic_from_profiles("attention.cu", f"attn_fwd_fp8:{name}")
+    tr16 = traffic_from_profiles("attention.cu", f"attn_fwd_bf16:{name}")
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(name, 12.0, had)
+    line = {
+        "metric": METRIC, "value": v8, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": t8, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3", "data": "synthetic (seeded Gaussian N(0,1), drawn in bf16, quantised per 128-token block)",
+        "config": {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "Dqk": w.Dqk, "Dv": w.Dv,
+                   "path": "fp8: quantise Q,K,V (3 launches) + fp8 causal attention (1 launch)",
+                   "hadamard": had, "parallelism": f"replicas x{world}",
+                   "l2": "256 MiB flush between timed steps; inputs larger than L2"},
+        "pct_of_peak": {"fp8_attention_kernel": a8 / fp8_peak, "fp8_step": v8 / world / fp8_peak,
+                        "bf16_attention_kernel": a16 / peaks["bf16_tflops"],
+                        "peak_source": f"{src} (fp8 = bf16 x {FP8_PER_BF16:g}, nominal ratio)"},
+        "roofline": {"bound": "tensor", "achieved": a8, "peak": fp8_peak, "unit": UNIT, "frac": a8 / fp8_peak,
+                     "traffic": tr8, "kernel": "attn_fwd_fp8",
+                     "peak_note": f"dense fp8 = {src} bf16 burst {peaks['bf16_tflops']:g} x {FP8_PER_BF16:g} (of {src}); "
+                                  f"sustained-peak frac {a8 / fp8_peak_sus:.3f}",
+                     "ms_per_launch": t8k},
+        "bf16": {"value": v16, "unit": UNIT, "ms_per_step": t16, "dtype": "bf16", "gpu_launches": K,
+                 "roofline": {"bound": "tensor", "achieved": a16, "peak": peaks["bf16_tflops"], "unit": UNIT,
+                              "frac": a16 / peaks["bf16_tflops"], "traffic": tr16, "kernel": "attn_fwd_bf16",
+                              "peak_note": f"bf16 burst (of {src}); sustained-peak frac "
+                                           f"{a16 / peaks['bf16_tflops_sustained']:.3f}"}},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": None if cpu is None else {
+            "value": cpu["value"], "unit": UNIT, "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -35,6 +35,7 @@
 // records a code in the device status word, drains in-flight copies and
 // tensor-core work, frees its tensor memory and exits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -42,12 +43,21 @@
 namespace zyfa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;              // 3 warpgroups: softmax A, softmax B, loader/MMA
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split per path (launch: 384 x 168 = 64512 registers). FP8: the
+// softmax warpgroups take 224 and the loader/MMA warpgroup 56
+// (8*32*224 + 4*32*56 = 64512). BF16 keeps the even 168 split, which
+// measured faster for it.
+template <bool FP8>
+struct RegSplit {
+  static constexpr uint32_t kSoftmax = FP8 ? 224 : 168;
+  static constexpr uint32_t kControl = FP8 ? 56 : 168;
+  static_assert(8 * 32 * kSoftmax + 4 * 32 * kControl <= 384 * 168, "register split exceeds the launch");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // BF16: keep a stale max while x - m <= 8
-constexpr float kMaxBlockShift = 100.0f;    // FP8: bound on the per-tile exponent k
 
 enum StatusCode : unsigned int {
   kStatusLoaderTimeout = 0x1u,
@@ -55,6 +65,22 @@ enum StatusCode : unsigned int {
   kStatusSoftmaxTimeout = 0x4u,
   kStatusDrainFailed = 0x100u,
 };
+
+// Optional timeline trace for performance work (compile with -DZYFA_TRACE):
+// CTA 0 records (clock64 << 8 | event) per role into a device buffer that
+// zyfa_trace_read() copies out. Not part of the normal build.
+#ifdef ZYFA_TRACE
+constexpr int kTraceLen = 8192;
+__device__ unsigned long long zyfa_trace_buf[4][kTraceLen];
+__device__ __forceinline__ void trace_ev(int role, uint32_t& idx, uint32_t code) {
+  if (blockIdx.x == 0 && idx < kTraceLen) zyfa_trace_buf[role][idx++] = (clock64() << 8) | code;
+}
+#define ZTRACE(role, idx, code) trace_ev(role, idx, code)
+#else
+#define ZTRACE(role, idx, code) \
+  do {                          \
+  } while (0)
+#endif
 
 template <int DQK, bool FP8>
 struct Cfg {
@@ -69,8 +95,10 @@ struct Cfg {
   static constexpr int kPvSteps = FP8 ? 4 : 8;                  // 128 keys / MMA K
   static constexpr int kPvStepBytes = (FP8 ? 32 : 16) * 128;    // V rows per MMA K step
   static constexpr int kInnerElts = 128 / kElt;                 // TMA box inner extent
-  static constexpr int kNK = FP8 ? (DQK == 128 ? 4 : 3) : (DQK == 128 ? 3 : 2);
-  static constexpr int kNV = FP8 ? (DQK == 128 ? 4 : 3) : (DQK == 128 ? 2 : 1);
+  // Ring depths. K_j is released one iteration before V_j (after the second
+  // tile's S MMA versus its PV MMA), so V gets the deeper ring.
+  static constexpr int kNK = FP8 ? (DQK == 128 ? 4 : 3) : 2;
+  static constexpr int kNV = FP8 ? (DQK == 128 ? 6 : 4) : (DQK == 128 ? 3 : 1);
   static constexpr uint32_t kIdescS = make_idesc(128, 128, FP8 ? 0u : 1u, false);
   static constexpr uint32_t kIdescPV = make_idesc(128, kDv, FP8 ? 0u : 1u, true);
   static constexpr int kOffQ = 0;
@@ -129,10 +157,19 @@ struct Smem {
   __device__ __forceinline__ uint8_t* v_tile(int s) const { return base + C::kOffV + s * C::kVTileBytes; }
 };
 
+// Warp-wide bounded wait: every lane polls; the result is uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* status, unsigned int code, uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status, code, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ loader --
+// The whole warp runs the loop (so addresses and coordinates stay uniform);
+// one elected lane issues the TMA copies and the expect-tx arrivals.
 template <int DQK, bool FP8>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                            const CUtensorMap* tm_v, const AttnArgs& a, int n_qtiles) {
+                            const CUtensorMap* tm_v, const AttnArgs& a, int n_qtiles, bool leader) {
   using C = Cfg<DQK, FP8>;
   const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
   const int group = a.Hq / a.Hkv;
@@ -140,41 +177,53 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   int ks = 0, vs = 0;
   uint32_t kph = 0, vph = 0, qn = 0;
   uint32_t k_issued = 0, v_issued = 0;          // stages written at least once
-  uint32_t k_par[C::kNK], v_par[C::kNV];
+  uint32_t k_par = 0, v_par = 0;                // parity bit of each stage's last issue
   bool ok = true;
+  uint32_t tix = 0;
+  (void)tix;
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(u, a.B, a.Hq, n_qtiles);
     const int hkv = w.hq / group;
-    if (!(ok = mbar_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
+    if (!(ok = warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
       break;
-    mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
-#pragma unroll
-    for (int kb = 0; kb < C::kQkBlocks; ++kb)
-      tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, 2 * w.t * 128, w.b);
-    if (w.has_b) {
+    if (leader) {
+      mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
 #pragma unroll
       for (int kb = 0; kb < C::kQkBlocks; ++kb)
-        tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, (2 * w.t + 1) * 128,
-                    w.b);
+        tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, 2 * w.t * 128, w.b);
+      if (w.has_b) {
+#pragma unroll
+        for (int kb = 0; kb < C::kQkBlocks; ++kb)
+          tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, (2 * w.t + 1) * 128,
+                      w.b);
+      }
     }
     ++qn;
     for (int j = 0; j < w.n_kv; ++j) {
-      if (!(ok = mbar_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
+      if (leader) ZTRACE(3, tix, 20);
+      if (!(ok = warp_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
         break;
-      mbar_arrive_expect_tx(sm.k_full(ks), C::kQkTileBytes);
+      if (leader) {
+        ZTRACE(3, tix, 21);
+        mbar_arrive_expect_tx(sm.k_full(ks), C::kQkTileBytes);
 #pragma unroll
-      for (int kb = 0; kb < C::kQkBlocks; ++kb)
-        tma_load_4d(sm.k_tile(ks) + kb * 16384, tm_k, sm.k_full(ks), kb * C::kInnerElts, hkv, j * 128, w.b);
-      k_par[ks] = kph;
+        for (int kb = 0; kb < C::kQkBlocks; ++kb)
+          tma_load_4d(sm.k_tile(ks) + kb * 16384, tm_k, sm.k_full(ks), kb * C::kInnerElts, hkv, j * 128, w.b);
+      }
+      k_par = (k_par & ~(1u << ks)) | (kph << ks);
       k_issued |= 1u << ks;
       if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
-      if (!(ok = mbar_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
+      if (leader) ZTRACE(3, tix, 22);
+      if (!(ok = warp_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
         break;
-      mbar_arrive_expect_tx(sm.v_full(vs), C::kVTileBytes);
+      if (leader) {
+        ZTRACE(3, tix, 23);
+        mbar_arrive_expect_tx(sm.v_full(vs), C::kVTileBytes);
 #pragma unroll
-      for (int vb = 0; vb < C::kVBlocks; ++vb)
-        tma_load_4d(sm.v_tile(vs) + vb * 16384, tm_v, sm.v_full(vs), vb * C::kInnerElts, hkv, j * 128, w.b);
-      v_par[vs] = vph;
+        for (int vb = 0; vb < C::kVBlocks; ++vb)
+          tma_load_4d(sm.v_tile(vs) + vb * 16384, tm_v, sm.v_full(vs), vb * C::kInnerElts, hkv, j * 128, w.b);
+      }
+      v_par = (v_par & ~(1u << vs)) | (vph << vs);
       v_issued |= 1u << vs;
       if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
     }
@@ -183,72 +232,93 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
     // Tail: wait until every stage has been released for the last time, so
     // no tcgen05.commit arrival is still in flight when the CTA exits.
     for (int i = 0; i < C::kNK; ++i) {
-      if (!mbar_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
+      if (!warp_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
       if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
     }
     for (int i = 0; i < C::kNV; ++i) {
-      if (!mbar_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
+      if (!warp_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
       if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
     }
-    mbar_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns);
-  } else {
-    // Abort: let every copy this thread issued land before the CTA exits.
+    warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns);
+  } else if (leader) {
+    // Abort: let every copy this warp issued land before the CTA exits.
     constexpr uint64_t kDrainNs = 200000000ull;
     for (int s = 0; s < C::kNK; ++s)
       if ((k_issued >> s) & 1u)
-        if (!mbar_wait_drain(sm.k_full(s), k_par[s], kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
+        if (!mbar_wait_drain(sm.k_full(s), (k_par >> s) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
     for (int s = 0; s < C::kNV; ++s)
       if ((v_issued >> s) & 1u)
-        if (!mbar_wait_drain(sm.v_full(s), v_par[s], kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
+        if (!mbar_wait_drain(sm.v_full(s), (v_par >> s) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
     if (qn > 0)
       if (!mbar_wait_drain(sm.q_full(), (qn - 1) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
   }
 }
 
 // --------------------------------------------------------------------- MMA --
+// Operand descriptors are precomputed per buffer (Q tiles, K stages, V
+// stages are at fixed offsets); a K step only adds a constant to the low word.
+struct OperandDescs {
+  Desc q0;        // Q tile 0; tile 1 is kQkTileBytes further
+  Desc k0;        // K stage 0; stage s is s * kQkTileBytes further
+  Desc v0;        // V stage 0; stage s is s * kVTileBytes further
+};
+
 template <int DQK, bool FP8>
-__device__ __forceinline__ void issue_s(const Smem<DQK, FP8>& sm, uint32_t tmem_s, int qtile, int kstage) {
+__device__ __forceinline__ void issue_s(const OperandDescs& od, uint32_t tmem_s, int qtile, int kstage) {
   using C = Cfg<DQK, FP8>;
-  const uint32_t a_base = smem_u32(sm.q_tile(qtile));
-  const uint32_t b_base = smem_u32(sm.k_tile(kstage));
+  const uint32_t alo = od.q0.lo + static_cast<uint32_t>(qtile) * (C::kQkTileBytes >> 4);
+  const uint32_t blo = od.k0.lo + static_cast<uint32_t>(kstage) * (C::kQkTileBytes >> 4);
 #pragma unroll
   for (int st = 0; st < C::kQkSteps; ++st) {
-    const uint32_t off = (st * 32 / 128) * 16384 + (st * 32) % 128;
-    const uint64_t ad = smem_desc_sw128(a_base + off, 16, 1024);
-    const uint64_t bd = smem_desc_sw128(b_base + off, 16, 1024);
-    if constexpr (FP8) mma_ss_f8(tmem_s, ad, bd, C::kIdescS, st > 0 ? 1u : 0u);
-    else mma_ss_bf16(tmem_s, ad, bd, C::kIdescS, st > 0 ? 1u : 0u);
+    const uint32_t adv = static_cast<uint32_t>(((st * 32 / 128) * 16384 + (st * 32) % 128) >> 4);
+    if constexpr (FP8) mma_ss_f8_h(tmem_s, alo + adv, od.q0.hi, blo + adv, od.k0.hi, C::kIdescS, st > 0 ? 1u : 0u);
+    else mma_ss_bf16_h(tmem_s, alo + adv, od.q0.hi, blo + adv, od.k0.hi, C::kIdescS, st > 0 ? 1u : 0u);
   }
 }
 
 template <int DQK, bool FP8>
-__device__ __forceinline__ void issue_pv(const Smem<DQK, FP8>& sm, uint32_t tmem_p, uint32_t tmem_o, int vstage,
+__device__ __forceinline__ void issue_pv(const OperandDescs& od, uint32_t tmem_p, uint32_t tmem_o, int vstage,
                                          bool accumulate) {
   using C = Cfg<DQK, FP8>;
-  const uint32_t b_base = smem_u32(sm.v_tile(vstage));
+  // V is [keys, dv] with dv contiguous: an MN-major B operand. LBO steps
+  // between 128-byte dv column blocks, SBO between 8-key row groups.
+  const uint32_t blo = od.v0.lo + static_cast<uint32_t>(vstage) * (C::kVTileBytes >> 4);
 #pragma unroll
   for (int st = 0; st < C::kPvSteps; ++st) {
-    // V is [keys, dv] with dv contiguous: an MN-major B operand. LBO steps
-    // between 128-byte dv column blocks, SBO between 8-key row groups.
-    const uint64_t bd = smem_desc_sw128(b_base + st * C::kPvStepBytes, 16384, 1024);
     const uint32_t acc = (accumulate || st > 0) ? 1u : 0u;
-    if constexpr (FP8) mma_ts_f8(tmem_o, tmem_p + st * 8, bd, C::kIdescPV, acc);
-    else mma_ts_bf16(tmem_o, tmem_p + st * 8, bd, C::kIdescPV, acc);
+    const uint32_t adv = static_cast<uint32_t>((st * C::kPvStepBytes) >> 4);
+    if constexpr (FP8) mma_ts_f8_h(tmem_o, tmem_p + st * 8, blo + adv, od.v0.hi, C::kIdescPV, acc);
+    else mma_ts_bf16_h(tmem_o, tmem_p + st * 8, blo + adv, od.v0.hi, C::kIdescPV, acc);
   }
 }
 
+// The whole warp runs the schedule (waits, stage and phase bookkeeping,
+// descriptors: all warp-uniform); one elected lane issues tcgen05.mma and
+// tcgen05.commit, so a commit tracks exactly the MMAs of that lane.
 template <int DQK, bool FP8>
-__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, int n_qtiles) {
+__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, int n_qtiles, bool leader) {
   using C = Cfg<DQK, FP8>;
   const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
   volatile int* abort_flag = sm.abort_flag();
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 384};
+  const uint32_t tS0 = tmem, tS1 = tmem + 128;
+  const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
   int ks = 0, vs = 0;
   uint32_t kph = 0, vph = 0, qn = 0, pph0 = 0, pph1 = 0;
   bool ok = true;
-#define ZYFA_WAIT(bar, par)                                                                          \
-  if (!(ok = mbar_wait((bar), (par), abort_flag, a.status, kStatusMmaTimeout, a.timeout_ns))) break; \
+  OperandDescs od;
+  od.q0 = make_desc_sw128(smem_u32(sm.q_tile(0)), 16, 1024);
+  od.k0 = make_desc_sw128(smem_u32(sm.k_tile(0)), 16, 1024);
+  od.v0 = make_desc_sw128(smem_u32(sm.v_tile(0)), 16384, 1024);
+  uint32_t tix = 0;
+  (void)tix;
+// Waits on TMA barriers need no tcgen05 fence (the mbarrier orders the copy
+// before the MMA's shared-memory reads); waits on P (written to tensor memory
+// by the softmax warps with tcgen05.st) are followed by
+// tcgen05.fence::after_thread_sync.
+#define ZYFA_WAIT(bar, par) \
+  if (!(ok = warp_wait((bar), (par), abort_flag, a.status, kStatusMmaTimeout, a.timeout_ns))) break;
+#define ZYFA_WAIT_P(bar, par)                                                                         \
+  if (!(ok = warp_wait((bar), (par), abort_flag, a.status, kStatusMmaTimeout, a.timeout_ns))) break; \
   tc_fence_after();
 
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -257,75 +327,159 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
       ZYFA_WAIT(sm.k_full(ks), kph);
-      issue_s(sm, tS[0], 0, ks);
-      tc_commit(sm.s_full(0));
-      if (w.has_b) {
-        issue_s(sm, tS[1], 1, ks);
-        tc_commit(sm.s_full(1));
+      if (leader) {
+        issue_s<DQK, FP8>(od, tS0, 0, ks);
+        tc_commit(sm.s_full(0));
+        if (w.has_b) {
+          issue_s<DQK, FP8>(od, tS1, 1, ks);
+          tc_commit(sm.s_full(1));
+        }
+        tc_commit(sm.k_empty(ks));
+        if (w.n_kv == 1) tc_commit(sm.q_empty());
       }
-      tc_commit(sm.k_empty(ks));
       if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
-      if (w.n_kv == 1) tc_commit(sm.q_empty());
       for (int j = 0; j < w.n_kv; ++j) {
+        if (leader) ZTRACE(2, tix, 10);
+#ifdef ZYFA_TRACE
+        if (leader) ZTRACE(2, tix, mbar_test(sm.v_full(vs), vph) ? 24 : 25);
+#endif
         ZYFA_WAIT(sm.v_full(vs), vph);
+        if (leader) ZTRACE(2, tix, 11);
         bool k_next = false;
         if (j < w.n_a) {
-          ZYFA_WAIT(sm.p_full(0), pph0);
+          if (leader) ZTRACE(2, tix, 12);
+          ZYFA_WAIT_P(sm.p_full(0), pph0);
+          if (leader) ZTRACE(2, tix, 13);
           pph0 ^= 1u;
-          issue_pv(sm, tS[0], tO[0], vs, j > 0);
+          if (leader) issue_pv<DQK, FP8>(od, tS0, tO0, vs, j > 0);
           if (j + 1 < w.n_a) {
+            if (leader) ZTRACE(2, tix, 18);
             ZYFA_WAIT(sm.k_full(ks), kph);
+            if (leader) ZTRACE(2, tix, 19);
             k_next = true;
-            issue_s(sm, tS[0], 0, ks);
-            tc_commit(sm.s_full(0));
-            if (!w.has_b && j + 1 == w.n_a - 1) tc_commit(sm.q_empty());
-          } else {
+            if (leader) {
+              issue_s<DQK, FP8>(od, tS0, 0, ks);
+              tc_commit(sm.s_full(0));
+              if (!w.has_b && j + 1 == w.n_a - 1) tc_commit(sm.q_empty());
+            }
+          } else if (leader) {
             tc_commit(sm.o_full(0));
           }
+          if (leader) ZTRACE(2, tix, 14);
         }
         if (w.has_b) {
-          ZYFA_WAIT(sm.p_full(1), pph1);
+          if (leader) ZTRACE(2, tix, 15);
+          ZYFA_WAIT_P(sm.p_full(1), pph1);
+          if (leader) ZTRACE(2, tix, 16);
           pph1 ^= 1u;
-          issue_pv(sm, tS[1], tO[1], vs, j > 0);
+          if (leader) issue_pv<DQK, FP8>(od, tS1, tO1, vs, j > 0);
           if (j + 1 < w.n_b) {
             if (!k_next) {
               ZYFA_WAIT(sm.k_full(ks), kph);
               k_next = true;
             }
-            issue_s(sm, tS[1], 1, ks);
-            tc_commit(sm.s_full(1));
-            if (j + 1 == w.n_b - 1) tc_commit(sm.q_empty());
-          } else {
+            if (leader) {
+              issue_s<DQK, FP8>(od, tS1, 1, ks);
+              tc_commit(sm.s_full(1));
+              if (j + 1 == w.n_b - 1) tc_commit(sm.q_empty());
+            }
+          } else if (leader) {
             tc_commit(sm.o_full(1));
           }
+          if (leader) ZTRACE(2, tix, 17);
         }
-        tc_commit(sm.v_empty(vs));
+        if (leader) tc_commit(sm.v_empty(vs));
         if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
         if (k_next) {
-          tc_commit(sm.k_empty(ks));
+          if (leader) tc_commit(sm.k_empty(ks));
           if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
         }
       }
     } while (false);
   }
 #undef ZYFA_WAIT
+#undef ZYFA_WAIT_P
   // Let every issued MMA (and the arrivals of earlier commits) complete.
-  tc_commit(sm.drain());
-  if (!mbar_wait_drain(sm.drain(), 0, 200000000ull)) atomicOr(a.status, kStatusDrainFailed);
+  if (leader) {
+    tc_commit(sm.drain());
+    if (!mbar_wait_drain(sm.drain(), 0, 200000000ull)) atomicOr(a.status, kStatusDrainFailed);
+  }
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------- softmax --
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
-// Exact sum of four e4m3 codes (bytes of w) scaled by 2^-120: each byte moved
-// to bits 20..27 is the float with the same value times 2^-120 (normals and
-// subnormals alike), so the fp32 additions of up to 128 such terms are exact.
-__device__ __forceinline__ float e4m3x4_sum_scaled(uint32_t w) {
-  const float f0 = __uint_as_float((w << 20) & 0x0FF00000u);
-  const float f1 = __uint_as_float((w << 12) & 0x0FF00000u);
-  const float f2 = __uint_as_float((w << 4) & 0x0FF00000u);
-  const float f3 = __uint_as_float((w >> 4) & 0x0FF00000u);
-  return __fadd_rn(__fadd_rn(f0, f1), __fadd_rn(f2, f3));
+// Row maximum of 128 scores: eight independent chains of 3-input max.
+__device__ __forceinline__ float row_max(const uint32_t (&s)[128]) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fmaxf(u2f(s[i]), u2f(s[8 + i]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = max3f(a[i], u2f(s[c + i]), u2f(s[c + 8 + i]));
+  }
+  return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
+// -inf above the diagonal for the 32 scores of columns col0..col0+31.
+__device__ __forceinline__ void mask_chunk(uint32_t* s, int col0, int r) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    if (col0 + c > r) s[c] = 0xff800000u;
+}
+
+// Exact sums of the four e4m3 codes in w: (v0 + v2, v1 + v3). Each pair of
+// codes is widened to f16 (exact: e4m3 is a subset of f16) and then to fp32,
+// where every value, subnormal codes included, is a normal number; sums of up
+// to 128 such values are exact in fp32.
+__device__ __forceinline__ float2 e4m3x4_pairsum(uint32_t w) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  return __fadd2_rn(a, b);
+}
+
+// Probabilities of one 32-column chunk c, p = 2^(s * ca + cb):
+//   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the fp32 p.
+//   FP8:  e4m3 codes, four per word, into pk[8c .. 8c+7]; acc sums the
+//         rounded values.
+// mxa tracks the raw score maximum.
+template <bool FP8>
+__device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, float cb, uint32_t* pk,
+                                            float2 (&acc)[2], float (&mxa)[2]) {
+  const float2 a2 = make_float2(ca, ca);
+  const float2 b2 = make_float2(cb, cb);
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float s0 = u2f(s[2 * i]), s1 = u2f(s[2 * i + 1]);
+      mxa[i & 1] = max3f(mxa[i & 1], s0, s1);
+      const float2 x = __ffma2_rn(make_float2(s0, s1), a2, b2);
+      const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      pk[16 * c + i] = pack_bf16x2(p.x, p.y);
+      acc[i & 1] = __fadd2_rn(acc[i & 1], p);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float s0 = u2f(s[4 * i]), s1 = u2f(s[4 * i + 1]), s2 = u2f(s[4 * i + 2]), s3 = u2f(s[4 * i + 3]);
+      mxa[0] = max3f(mxa[0], s0, s1);
+      mxa[1] = max3f(mxa[1], s2, s3);
+      const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
+      const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
+      const uint32_t w = pack_e4m3x4(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y));
+      pk[8 * c + i] = w;
+      acc[i & 1] = __fadd2_rn(acc[i & 1], e4m3x4_pairsum(w));
+    }
+  }
 }
 
 __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
@@ -339,6 +493,13 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
   }
 }
 
+// FP8 offset window. With offset o the rounded probabilities are
+// P' = e4m3(2^(x + log2 sv - o)). A tile whose largest P', 2^(bm - o), falls
+// outside [2^kWinLo, 2^kWinHi] moves o to bm - kWinCentre (and O, l are
+// rescaled); o never drops below the row's largest log2 value minus
+// kFloorBinades (blocks that far down underflow harmlessly).
+constexpr float kWinLo = -2.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
+
 template <int DQK, bool FP8>
 __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, int n_qtiles,
                              int warp, int lane) {
@@ -351,7 +512,12 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + wg * 128 + lane_off;
   const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
+  constexpr int kPk = FP8 ? 32 : 64;
   uint32_t sph = 0, oph = 0;
+  uint32_t tix = 0;
+  const bool tr = lane == 0 && (warp & 3) == 0;
+  (void)tix;
+  (void)tr;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o);
 
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -360,7 +526,10 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const int qt = 2 * w.t + wg;
     const int n = qt + 1;
     const int hkv = w.hq / group;
-    float m = 0.f, l = 0.f, R = 1.f;
+    // BF16: m = running max in log2 units (kept while a new maximum stays
+    //       within 2^8 of it), l = sum of the fp32 probabilities.
+    // FP8:  m = offset o, top = largest log2(p * sv) seen, l = sum of P'/sv.
+    float m = 0.f, l = 0.f, top = 0.f;
     float sq = 1.f;
     const float* ks_row = nullptr;
     const float* vs_row = nullptr;
@@ -370,120 +539,119 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       vs_row = a.v_scale + (static_cast<int64_t>(w.b) * a.Hkv + hkv) * nblk;
     }
     for (int j = 0; j < n; ++j) {
-      float sk = 1.f, sv = 1.f;
+      float cj = a.scale_log2, lsv = 0.f, inv_sv = 1.f;
       if constexpr (FP8) {
-        sk = __ldg(ks_row + j);
-        sv = __ldg(vs_row + j);
+        const float sk = __ldg(ks_row + j);
+        const float sv = __ldg(vs_row + j);
+        cj = sq * sk * a.scale_log2;
+        lsv = __log2f(sv);
+        inv_sv = 1.0f / sv;
       }
+      if (tr) ZTRACE(wg, tix, 1);
       bool ok = mbar_wait(sm.s_full(wg), sph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return; }
       sph ^= 1u;
       tc_fence_after();
-      uint32_t s[128];
+      if (tr) ZTRACE(wg, tix, 2);
+      const bool diag = (j == n - 1);
+      uint32_t pk[kPk];
+      float psum = 0.f;
+      bool first = (j == 0);
+      bool redone = false;
+      for (;;) {
+        uint32_t s[128];
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float mxa[2] = {-INFINITY, -INFINITY};
+        if (first) {
+          // First tile of the row: the maximum is needed before any exponential.
+          tmem_ld128(tS, s);
+          if (diag) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
-      if (j == n - 1) {
+            for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
+          }
+          const float mx0 = row_max(s);
+          if constexpr (FP8) {
+            top = mx0 * cj + lsv;
+            m = top - kWinCentre;
+          } else {
+            m = mx0 * cj;
+          }
+          const float cb = FP8 ? (lsv - m) : -m;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > r) s[c] = 0xff800000u;   // -inf above the diagonal
-      }
-      float mx = u2f(s[0]);
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, u2f(s[c]));
-
-      if constexpr (!FP8) {
-        const float xmax = mx * a.scale_log2;
-        float rho = 1.f;
-        bool need = false;
-        if (j == 0) {
-          m = xmax;
-        } else if (xmax > m + kRescaleThreshold) {
-          rho = ex2_approx(m - xmax);
-          m = xmax;
-          need = true;
-        }
-        l *= rho;
-        const float neg = -m;
-        uint32_t pk[64];
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(fmaf(u2f(s[2 * c]), a.scale_log2, neg));
-          const float p1 = ex2_approx(fmaf(u2f(s[2 * c + 1]), a.scale_log2, neg));
-          const float p2 = ex2_approx(fmaf(u2f(s[2 * c + 2]), a.scale_log2, neg));
-          const float p3 = ex2_approx(fmaf(u2f(s[2 * c + 3]), a.scale_log2, neg));
-          l0 += p0; l1 += p1; l2 += p2; l3 += p3;
-          pk[c] = pack_bf16x2(p0, p1);
-          pk[c + 1] = pack_bf16x2(p2, p3);
-        }
-        l += (l0 + l1) + (l2 + l3);
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        if (j > 0 && __any_sync(0xffffffffu, need)) rescale_o_row(tO, rho);
-      } else {
-        const float cj = sq * sk * a.scale_log2;
-        const float xmax = mx * cj;
-        const float m_new = (j == 0) ? xmax : fmaxf(m, xmax);
-        const float kf = fminf(floorf(m_new - xmax), kMaxBlockShift);   // 2^k lifts the tile max into (0.5, 1]
-        const int ki = static_cast<int>(kf);
-        const float off = m_new - kf;
-        uint32_t pk[32];
-        float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(u2f(s[4 * i]), cj, -off));
-          const float p1 = ex2_approx(fmaf(u2f(s[4 * i + 1]), cj, -off));
-          const float p2 = ex2_approx(fmaf(u2f(s[4 * i + 2]), cj, -off));
-          const float p3 = ex2_approx(fmaf(u2f(s[4 * i + 3]), cj, -off));
-          pk[i] = pack_e4m3x4(p0, p1, p2, p3);
-          if (i & 1) l1 = __fadd_rn(l1, e4m3x4_sum_scaled(pk[i]));
-          else l0 = __fadd_rn(l0, e4m3x4_sum_scaled(pk[i]));
-        }
-        const float lsum = __fadd_rn(l0, l1);                              // sum of rounded P, times 2^-120
-        const float two_m_k = __int_as_float((127 - ki) << 23);           // 2^-k
-        const float lift = __int_as_float((127 + 120 - ki) << 23);        // 2^(120-k)
-        const float r_new = sv * two_m_k;
-        float rho = 1.f;
-        if (j == 0) {
-          l = lsum * lift;
+          for (int c = 0; c < 4; ++c) probs_chunk<FP8>(c, &s[32 * c], cj, cb, pk, acc, mxa);
         } else {
-          const float decay = ex2_approx(m - m_new);
-          rho = (R / r_new) * decay;
-          l = fmaf(l, decay, lsum * lift);
+          // Later tiles: exponentials with the current offset, S read in
+          // 32-column chunks.
+          const float cb = FP8 ? (lsv - m) : -m;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+            if (diag) mask_chunk(&s[32 * c], 32 * c, r);
+            probs_chunk<FP8>(c, &s[32 * c], cj, cb, pk, acc, mxa);
+          }
         }
+        const float2 t = __fadd2_rn(acc[0], acc[1]);
+        psum = t.x + t.y;
+        if (first || redone) break;
+        // Check the offset against this tile's maximum; redo the (rare) rows
+        // that need a new one. S is intact: P has not been written yet.
+        const float mx = fmaxf(mxa[0], mxa[1]);
+        bool need;
+        float m_new;
+        if constexpr (FP8) {
+          const float bm = mx * cj + lsv;
+          const float rel = bm - m;
+          need = rel > kWinHi || (rel < kWinLo && bm > top - kFloorBinades);
+          m_new = need ? fmaxf(bm - kWinCentre, fmaxf(top, bm) - kFloorBinades) : m;
+          top = fmaxf(top, bm);
+        } else {
+          const float xmax = mx * cj;
+          need = xmax > m + kRescaleThreshold;
+          m_new = need ? xmax : m;
+        }
+        if (!__any_sync(0xffffffffu, need)) break;
+        const float rho = ex2_approx(m - m_new);
+        l *= rho;
         m = m_new;
-        R = r_new;
-        tmem_st32(tS, pk);
-        if (j > 0) rescale_o_row(tO, rho);
+        rescale_o_row(tO, rho);
+        redone = true;
       }
+      if (tr) ZTRACE(wg, tix, 3);
+      if constexpr (FP8) l = fmaf(psum, inv_sv, l);
+      else l += psum;
+#pragma unroll
+      for (int c = 0; c < kPk / 32; ++c) tmem_st32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * c]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.p_full(wg));
+      if (tr) ZTRACE(wg, tix, 4);
     }
 
-    // epilogue: O / l (FP8: times the accumulator scale R), BF16, global store
+    // epilogue: O / l, BF16, global store
+    if (tr) ZTRACE(wg, tix, 5);
     bool ok = mbar_wait(sm.o_full(wg), oph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
     if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return; }
     oph ^= 1u;
     tc_fence_after();
-    const float inv = FP8 ? (R / l) : (1.f / l);
+    const float inv = 1.f / l;
     const int q_row = qt * 128 + r;
     __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(q_row) * a.o_ss + w.hq * a.o_sh;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
-      __syncwarp();   // tcgen05.ld is warp-collective; the store below is per-thread
+      __syncwarp();   // tcgen05.ld is warp-collective; the stores below are per-thread
       tmem_ld32(tO + 32 * c, o);
-      uint32_t pk[16];
+      uint32_t pko[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
+      for (int e = 0; e < 16; ++e) pko[e] = pack_bf16x2(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
       if (q_row < a.S) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pko[4 * v], pko[4 * v + 1], pko[4 * v + 2], pko[4 * v + 3]);
       }
     }
+    if (tr) ZTRACE(wg, tix, 7);
   }
 }
 
@@ -528,13 +696,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot();
 
-  if (warp == kLoadWarp) {
-    if (lane == 0 && !a.debug_stall) loader_role(sm, &tm_q, &tm_k, &tm_v, a, n_qtiles);
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role(sm, tmem, a, n_qtiles);
+  if (warp >= 8) {
+    if constexpr (RegSplit<FP8>::kControl != 168) regs_decrease<RegSplit<FP8>::kControl>();
+    const bool leader = elect_one_sync();
+    if (warp == kLoadWarp) {
+      if (!a.debug_stall) loader_role(sm, &tm_q, &tm_k, &tm_v, a, n_qtiles, leader);
+    } else if (warp == kMmaWarp) {
+      mma_role(sm, tmem, a, n_qtiles, leader);
+    }
     __syncwarp();
   } else {
+    if constexpr (RegSplit<FP8>::kSoftmax != 168) regs_increase<RegSplit<FP8>::kSoftmax>();
     softmax_role(sm, tmem, a, n_qtiles, warp, lane);
     __syncwarp();
   }
@@ -577,3 +749,9 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
 }
 
 }  // namespace zyfa
+
+#ifdef ZYFA_TRACE
+extern "C" int zyfa_trace_read(void* dst, size_t bytes) {
+  return cudaMemcpyFromSymbol(dst, zyfa::zyfa_trace_buf, bytes) == cudaSuccess ? 0 : 3;
+}
+#endif
