@@ -118,14 +118,34 @@ struct Unit {
   int n_a, n_b, n_kv;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int n_qtiles) {
+// Work order. The (batch, KV head) groups are taken kGroupsInFlight at a
+// time; inside such a super-group the longest query-tile pairs come first and,
+// for each pair, the groups and then their query heads are adjacent. Units in
+// flight then share a few KV heads (K/V stay in L2) without every CTA
+// streaming the very same K/V tile at once.
+#ifndef ZYFA_GROUPS_IN_FLIGHT
+#define ZYFA_GROUPS_IN_FLIGHT 8
+#endif
+constexpr int kGroupsInFlight = ZYFA_GROUPS_IN_FLIGHT;
+
+__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles) {
   const int n_pairs = (n_qtiles + 1) / 2;
-  const int bh_count = B * Hq;
+  const int G = Hq / Hkv;
+  const int n_groups = B * Hkv;
+  const int per_sg = kGroupsInFlight * G * n_pairs;
+  const int sg = u / per_sg;
+  const int r = u - sg * per_sg;
+  const int gs_here = min(kGroupsInFlight, n_groups - sg * kGroupsInFlight);
+  const int per_t = gs_here * G;
+  const int tq = r / per_t;
+  const int rr = r - tq * per_t;
+  const int gi = rr / G;
+  const int group = sg * kGroupsInFlight + gi;
   Unit w;
-  w.t = n_pairs - 1 - u / bh_count;            // longest pairs first
-  const int bh = u % bh_count;
-  w.b = bh / Hq;
-  w.hq = bh % Hq;                               // heads of a GQA group adjacent
+  w.b = group / Hkv;
+  const int hkv = group - w.b * Hkv;
+  w.t = n_pairs - 1 - tq;
+  w.hq = hkv * G + (rr - gi * G);
   w.has_b = (2 * w.t + 1) < n_qtiles;
   w.n_a = 2 * w.t + 1;
   w.n_b = 2 * w.t + 2;
@@ -182,7 +202,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   uint32_t tix = 0;
   (void)tix;
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, n_qtiles);
+    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
     const int hkv = w.hq / group;
     if (!(ok = warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
       break;
@@ -322,7 +342,7 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
   tc_fence_after();
 
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, n_qtiles);
+    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
     do {
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
@@ -521,7 +541,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o);
 
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, n_qtiles);
+    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
     if (wg == 1 && !w.has_b) continue;
     const int qt = 2 * w.t + wg;
     const int n = qt + 1;
