@@ -358,32 +358,31 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
         if (w.n_kv == 1) tc_commit(sm.q_empty());
       }
       if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+      // The tensor pipe accepts about one MMA ahead of execution, so the
+      // issuing thread runs in step with it: every wait is done before a
+      // contiguous PV -> S issue block, never between two GEMMs.
       for (int j = 0; j < w.n_kv; ++j) {
+        const bool need_k = (j + 1 < w.n_kv);      // K_{j+1} feeds S_A(j+1) and/or S_B(j+1)
         if (leader) ZTRACE(2, tix, 10);
-#ifdef ZYFA_TRACE
-        if (leader) ZTRACE(2, tix, mbar_test(sm.v_full(vs), vph) ? 24 : 25);
-#endif
         ZYFA_WAIT(sm.v_full(vs), vph);
+        if (need_k) {
+          ZYFA_WAIT(sm.k_full(ks), kph);
+        }
         if (leader) ZTRACE(2, tix, 11);
-        bool k_next = false;
         if (j < w.n_a) {
           if (leader) ZTRACE(2, tix, 12);
           ZYFA_WAIT_P(sm.p_full(0), pph0);
           if (leader) ZTRACE(2, tix, 13);
           pph0 ^= 1u;
-          if (leader) issue_pv<DQK, FP8>(od, tS0, tO0, vs, j > 0);
-          if (j + 1 < w.n_a) {
-            if (leader) ZTRACE(2, tix, 18);
-            ZYFA_WAIT(sm.k_full(ks), kph);
-            if (leader) ZTRACE(2, tix, 19);
-            k_next = true;
-            if (leader) {
+          if (leader) {
+            issue_pv<DQK, FP8>(od, tS0, tO0, vs, j > 0);
+            if (j + 1 < w.n_a) {
               issue_s<DQK, FP8>(od, tS0, 0, ks);
               tc_commit(sm.s_full(0));
               if (!w.has_b && j + 1 == w.n_a - 1) tc_commit(sm.q_empty());
+            } else {
+              tc_commit(sm.o_full(0));
             }
-          } else if (leader) {
-            tc_commit(sm.o_full(0));
           }
           if (leader) ZTRACE(2, tix, 14);
         }
@@ -392,25 +391,21 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
           ZYFA_WAIT_P(sm.p_full(1), pph1);
           if (leader) ZTRACE(2, tix, 16);
           pph1 ^= 1u;
-          if (leader) issue_pv<DQK, FP8>(od, tS1, tO1, vs, j > 0);
-          if (j + 1 < w.n_b) {
-            if (!k_next) {
-              ZYFA_WAIT(sm.k_full(ks), kph);
-              k_next = true;
-            }
-            if (leader) {
+          if (leader) {
+            issue_pv<DQK, FP8>(od, tS1, tO1, vs, j > 0);
+            if (j + 1 < w.n_b) {
               issue_s<DQK, FP8>(od, tS1, 1, ks);
               tc_commit(sm.s_full(1));
               if (j + 1 == w.n_b - 1) tc_commit(sm.q_empty());
+            } else {
+              tc_commit(sm.o_full(1));
             }
-          } else if (leader) {
-            tc_commit(sm.o_full(1));
           }
           if (leader) ZTRACE(2, tix, 17);
         }
         if (leader) tc_commit(sm.v_empty(vs));
         if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
-        if (k_next) {
+        if (need_k) {
           if (leader) tc_commit(sm.k_empty(ks));
           if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
         }
