@@ -445,21 +445,29 @@ __device__ __forceinline__ void mask_chunk(uint32_t* s, int col0, int r) {
     if (col0 + c > r) s[c] = 0xff800000u;
 }
 
-// Exact sums of the four e4m3 codes in w: (v0 + v2, v1 + v3). Each pair of
-// codes is widened to f16 (exact: e4m3 is a subset of f16) and then to fp32,
-// where every value, subnormal codes included, is a normal number; sums of up
-// to 128 such values are exact in fp32.
-__device__ __forceinline__ float2 e4m3x4_pairsum(uint32_t w) {
-  uint32_t h01, h23;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(h01), "=r"(h23)
-      : "r"(w));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-  return __fadd2_rn(a, b);
+// Four floats -> four e4m3 codes (RNE, saturating; v0 in bits 0..7), and
+// acc += (v0' + v2', v1' + v3') over the rounded values v'. Each pair of codes
+// is widened to f16 (exact: e4m3 is a subset of f16) and added to the fp32
+// accumulator with a mixed-precision add, where every value, subnormal codes
+// included, is a normal number; sums of up to 128 such values are exact in
+// fp32 while they stay below 2^15.
+__device__ __forceinline__ uint32_t pack_e4m3x4_sum(float v0, float v1, float v2, float v3, float2& acc) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 h01, h23;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %4, %3;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %6, %5;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t"
+      "cvt.rn.f16x2.e4m3x2 h01, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h23, hi;\n\t"
+      "mov.b32 {a0, a1}, h01;\n\t"
+      "mov.b32 {a2, a3}, h23;\n\t"
+      "add.rn.f32.f16 %1, a0, %1;\n\t"
+      "add.rn.f32.f16 %2, a1, %2;\n\t"
+      "add.rn.f32.f16 %1, a2, %1;\n\t"
+      "add.rn.f32.f16 %2, a3, %2;\n\t}"
+      : "=r"(d), "+f"(acc.x), "+f"(acc.y)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return d;
 }
 
 // Probabilities of one 32-column chunk c, p = 2^(s * ca + cb):
@@ -490,9 +498,8 @@ __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, 
       mxa[1] = max3f(mxa[1], s2, s3);
       const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
       const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
-      const uint32_t w = pack_e4m3x4(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y));
-      pk[8 * c + i] = w;
-      acc[i & 1] = __fadd2_rn(acc[i & 1], e4m3x4_pairsum(w));
+      pk[8 * c + i] = pack_e4m3x4_sum(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y),
+                                      acc[i & 1]);
     }
   }
 }
@@ -577,27 +584,30 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         uint32_t s[128];
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float mxa[2] = {-INFINITY, -INFINITY};
-        if (first) {
-          // First tile of the row: the maximum is needed before any exponential.
+        if (first || FP8) {
+          // The whole row of S in one load: the first tile needs the maximum
+          // before any exponential; FP8 rows are short enough to hold it.
           tmem_ld128(tS, s);
           if (diag) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
           }
-          const float mx0 = row_max(s);
-          if constexpr (FP8) {
-            top = mx0 * cj + lsv;
-            m = top - kWinCentre;
-          } else {
-            m = mx0 * cj;
+          if (first) {
+            const float mx0 = row_max(s);
+            if constexpr (FP8) {
+              top = mx0 * cj + lsv;
+              m = top - kWinCentre;
+            } else {
+              m = mx0 * cj;
+            }
           }
           const float cb = FP8 ? (lsv - m) : -m;
 #pragma unroll
           for (int c = 0; c < 4; ++c) probs_chunk<FP8>(c, &s[32 * c], cj, cb, pk, acc, mxa);
         } else {
-          // Later tiles: exponentials with the current offset, S read in
-          // 32-column chunks.
-          const float cb = FP8 ? (lsv - m) : -m;
+          // BF16 later tiles: exponentials with the current offset, S read
+          // in 32-column chunks.
+          const float cb = -m;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));

@@ -336,17 +336,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
-// Four floats -> four e4m3 bytes (RNE, saturating to +-448); v0 in bits 0..7.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t}"
-      : "=r"(d)
-      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
-  return d;
-}
 // Two floats -> two e4m3 bytes (RNE, saturating); v0 in bits 0..7.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float v0, float v1) {
   uint16_t d;
