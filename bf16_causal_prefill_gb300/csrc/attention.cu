@@ -43,17 +43,19 @@
 namespace zyfa {
 namespace {
 
-constexpr int kThreads = 384;              // 3 warpgroups: softmax A, softmax B, loader/MMA
-constexpr int kLoadWarp = 8;
+constexpr int kThreads = 384;              // 3 warpgroups: softmax A, softmax B, loaders/MMA
+constexpr int kLoadWarp = 8;               // Q and K
 constexpr int kMmaWarp = 9;
-// Register split per path (launch: 384 x 168 = 64512 registers). FP8: the
-// softmax warpgroups take 224 and the loader/MMA warpgroup 56
-// (8*32*224 + 4*32*56 = 64512). BF16 keeps the even 168 split, which
-// measured faster for it.
+constexpr int kLoadWarpV = 10;             // V
+// Register split per path (launch: 384 x 168 = 64512 registers): the
+// softmax warpgroups take kSoftmax and the loader/MMA warpgroup kControl,
+// 8*32*kSoftmax + 4*32*kControl <= 64512. Measured on the 32K and 16K
+// workloads: 208/88 (FP8 and BF16) beats both the even split and
+// starving the control warps (which then spill inside the MMA issue loop).
 template <bool FP8>
 struct RegSplit {
-  static constexpr uint32_t kSoftmax = FP8 ? 224 : 168;
-  static constexpr uint32_t kControl = FP8 ? 56 : 168;
+  static constexpr uint32_t kSoftmax = 208;
+  static constexpr uint32_t kControl = 88;
   static_assert(8 * 32 * kSoftmax + 4 * 32 * kControl <= 384 * 168, "register split exceeds the launch");
 };
 constexpr uint32_t kTmemCols = 512;
@@ -95,8 +97,7 @@ struct Cfg {
   static constexpr int kPvSteps = FP8 ? 4 : 8;                  // 128 keys / MMA K
   static constexpr int kPvStepBytes = (FP8 ? 32 : 16) * 128;    // V rows per MMA K step
   static constexpr int kInnerElts = 128 / kElt;                 // TMA box inner extent
-  // Ring depths. K_j is released one iteration before V_j (after the second
-  // tile's S MMA versus its PV MMA), so V gets the deeper ring.
+  // Ring depths (K and V stages of 128 keys).
   static constexpr int kNK = FP8 ? (DQK == 128 ? 4 : 3) : 2;
   static constexpr int kNV = FP8 ? (DQK == 128 ? 6 : 4) : (DQK == 128 ? 3 : 1);
   static constexpr uint32_t kIdescS = make_idesc(128, 128, FP8 ? 0u : 1u, false);
@@ -185,91 +186,85 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ------------------------------------------------------------------ loader --
-// The whole warp runs the loop (so addresses and coordinates stay uniform);
-// one elected lane issues the TMA copies and the expect-tx arrivals.
-template <int DQK, bool FP8>
-__device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                            const CUtensorMap* tm_v, const AttnArgs& a, int n_qtiles, bool leader) {
+// Two loader warps: one streams Q and K, the other V. A thread's TMA copies
+// are processed one after another (one 16 KB tile takes ~430 cycles however
+// deep the ring is), so a single issuing thread caps the load rate near the
+// tensor pipe's demand; two issuers double it. Each warp runs its loop
+// uniformly (addresses and coordinates stay warp-uniform); one elected lane
+// issues the TMA copies and the expect-tx arrivals.
+enum LoadStream { kStreamQK = 0, kStreamV = 1 };
+
+template <int DQK, bool FP8, int STREAM>
+__device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
+                            const AttnArgs& a, int n_qtiles, bool leader) {
   using C = Cfg<DQK, FP8>;
+  constexpr bool kIsK = (STREAM == kStreamQK);
+  constexpr int kStages = kIsK ? C::kNK : C::kNV;
+  constexpr int kBlocks = kIsK ? C::kQkBlocks : C::kVBlocks;
+  constexpr uint32_t kTileBytes = kIsK ? C::kQkTileBytes : C::kVTileBytes;
   const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = sm.abort_flag();
-  int ks = 0, vs = 0;
-  uint32_t kph = 0, vph = 0, qn = 0;
-  uint32_t k_issued = 0, v_issued = 0;          // stages written at least once
-  uint32_t k_par = 0, v_par = 0;                // parity bit of each stage's last issue
+  int st = 0;
+  uint32_t ph = 0, qn = 0;
+  uint32_t issued = 0;        // stages written at least once
+  uint32_t par = 0;           // parity bit of each stage's last issue
   bool ok = true;
   uint32_t tix = 0;
   (void)tix;
+  auto full = [&](int i) { return kIsK ? sm.k_full(i) : sm.v_full(i); };
+  auto empty = [&](int i) { return kIsK ? sm.k_empty(i) : sm.v_empty(i); };
+  auto tile = [&](int i) { return kIsK ? sm.k_tile(i) : sm.v_tile(i); };
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
     const int hkv = w.hq / group;
-    if (!(ok = warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
-      break;
-    if (leader) {
-      mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
-#pragma unroll
-      for (int kb = 0; kb < C::kQkBlocks; ++kb)
-        tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, 2 * w.t * 128, w.b);
-      if (w.has_b) {
+    if constexpr (kIsK) {
+      if (!(ok = warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
+        break;
+      if (leader) {
+        mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
 #pragma unroll
         for (int kb = 0; kb < C::kQkBlocks; ++kb)
-          tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, (2 * w.t + 1) * 128,
-                      w.b);
+          tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, 2 * w.t * 128, w.b);
+        if (w.has_b) {
+#pragma unroll
+          for (int kb = 0; kb < C::kQkBlocks; ++kb)
+            tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq,
+                        (2 * w.t + 1) * 128, w.b);
+        }
       }
+      ++qn;
     }
-    ++qn;
     for (int j = 0; j < w.n_kv; ++j) {
-      if (leader) ZTRACE(3, tix, 20);
-      if (!(ok = warp_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
-        break;
+      if (leader) ZTRACE(3, tix, kIsK ? 20 : 22);
+      if (!(ok = warp_wait(empty(st), ph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns))) break;
       if (leader) {
-        ZTRACE(3, tix, 21);
-        mbar_arrive_expect_tx(sm.k_full(ks), C::kQkTileBytes);
+        ZTRACE(3, tix, kIsK ? 21 : 23);
+        mbar_arrive_expect_tx(full(st), kTileBytes);
 #pragma unroll
-        for (int kb = 0; kb < C::kQkBlocks; ++kb)
-          tma_load_4d(sm.k_tile(ks) + kb * 16384, tm_k, sm.k_full(ks), kb * C::kInnerElts, hkv, j * 128, w.b);
+        for (int kb = 0; kb < kBlocks; ++kb)
+          tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, j * 128, w.b);
       }
-      k_par = (k_par & ~(1u << ks)) | (kph << ks);
-      k_issued |= 1u << ks;
-      if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
-      if (leader) ZTRACE(3, tix, 22);
-      if (!(ok = warp_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
-        break;
-      if (leader) {
-        ZTRACE(3, tix, 23);
-        mbar_arrive_expect_tx(sm.v_full(vs), C::kVTileBytes);
-#pragma unroll
-        for (int vb = 0; vb < C::kVBlocks; ++vb)
-          tma_load_4d(sm.v_tile(vs) + vb * 16384, tm_v, sm.v_full(vs), vb * C::kInnerElts, hkv, j * 128, w.b);
-      }
-      v_par = (v_par & ~(1u << vs)) | (vph << vs);
-      v_issued |= 1u << vs;
-      if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
+      par = (par & ~(1u << st)) | (ph << st);
+      issued |= 1u << st;
+      if (++st == kStages) { st = 0; ph ^= 1u; }
     }
   }
   if (ok) {
     // Tail: wait until every stage has been released for the last time, so
     // no tcgen05.commit arrival is still in flight when the CTA exits.
-    for (int i = 0; i < C::kNK; ++i) {
-      if (!warp_wait(sm.k_empty(ks), kph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
-      if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+    for (int i = 0; i < kStages; ++i) {
+      if (!warp_wait(empty(st), ph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
+      if (++st == kStages) { st = 0; ph ^= 1u; }
     }
-    for (int i = 0; i < C::kNV; ++i) {
-      if (!warp_wait(sm.v_empty(vs), vph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)) break;
-      if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
-    }
-    warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns);
+    if constexpr (kIsK) warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns);
   } else if (leader) {
     // Abort: let every copy this warp issued land before the CTA exits.
     constexpr uint64_t kDrainNs = 200000000ull;
-    for (int s = 0; s < C::kNK; ++s)
-      if ((k_issued >> s) & 1u)
-        if (!mbar_wait_drain(sm.k_full(s), (k_par >> s) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
-    for (int s = 0; s < C::kNV; ++s)
-      if ((v_issued >> s) & 1u)
-        if (!mbar_wait_drain(sm.v_full(s), (v_par >> s) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
-    if (qn > 0)
+    for (int i = 0; i < kStages; ++i)
+      if ((issued >> i) & 1u)
+        if (!mbar_wait_drain(full(i), (par >> i) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
+    if (kIsK && qn > 0)
       if (!mbar_wait_drain(sm.q_full(), (qn - 1) & 1u, kDrainNs)) atomicOr(a.status, kStatusDrainFailed);
   }
 }
@@ -347,6 +342,7 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
       ZYFA_WAIT(sm.k_full(ks), kph);
+      if (leader) ZTRACE(2, tix, 26);
       if (leader) {
         issue_s<DQK, FP8>(od, tS0, 0, ks);
         tc_commit(sm.s_full(0));
@@ -365,8 +361,10 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
         const bool need_k = (j + 1 < w.n_kv);      // K_{j+1} feeds S_A(j+1) and/or S_B(j+1)
         if (leader) ZTRACE(2, tix, 10);
         ZYFA_WAIT(sm.v_full(vs), vph);
+        if (leader) ZTRACE(2, tix, 24);
         if (need_k) {
           ZYFA_WAIT(sm.k_full(ks), kph);
+          if (leader) ZTRACE(2, tix, 25);
         }
         if (leader) ZTRACE(2, tix, 11);
         if (j < w.n_a) {
@@ -470,6 +468,33 @@ __device__ __forceinline__ uint32_t pack_e4m3x4_sum(float v0, float v1, float v2
   return d;
 }
 
+#ifdef ZYFA_EX2_F16
+// Same, from f32 exponents: x rounded to f16 pairs, 2^x by the packed f16
+// exponential, then f16 pairs -> e4m3.
+__device__ __forceinline__ uint32_t exp2_e4m3x4_sum(float2 x01, float2 x23, float2& acc) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 x01, x23, e01, e23, h01, h23;\n\t"
+      "cvt.rn.f16x2.f32 x01, %4, %3;\n\t"
+      "cvt.rn.f16x2.f32 x23, %6, %5;\n\t"
+      "ex2.approx.f16x2 e01, x01;\n\t"
+      "ex2.approx.f16x2 e23, x23;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 lo, e01;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 hi, e23;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t"
+      "cvt.rn.f16x2.e4m3x2 h01, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h23, hi;\n\t"
+      "mov.b32 {a0, a1}, h01;\n\t"
+      "mov.b32 {a2, a3}, h23;\n\t"
+      "add.rn.f32.f16 %1, a0, %1;\n\t"
+      "add.rn.f32.f16 %2, a1, %2;\n\t"
+      "add.rn.f32.f16 %1, a2, %1;\n\t"
+      "add.rn.f32.f16 %2, a3, %2;\n\t}"
+      : "=r"(d), "+f"(acc.x), "+f"(acc.y)
+      : "f"(x01.x), "f"(x01.y), "f"(x23.x), "f"(x23.y));
+  return d;
+}
+#endif
+
 // Probabilities of one 32-column chunk c, p = 2^(s * ca + cb):
 //   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the fp32 p.
 //   FP8:  e4m3 codes, four per word, into pk[8c .. 8c+7]; acc sums the
@@ -498,8 +523,12 @@ __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, 
       mxa[1] = max3f(mxa[1], s2, s3);
       const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
       const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
+#ifdef ZYFA_EX2_F16
+      pk[8 * c + i] = exp2_e4m3x4_sum(x01, x23, acc[i & 1]);
+#else
       pk[8 * c + i] = pack_e4m3x4_sum(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y),
                                       acc[i & 1]);
+#endif
     }
   }
 }
@@ -722,16 +751,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_slot();
 
   if (warp >= 8) {
-    if constexpr (RegSplit<FP8>::kControl != 168) regs_decrease<RegSplit<FP8>::kControl>();
+    regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role(sm, &tm_q, &tm_k, &tm_v, a, n_qtiles, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK>(sm, &tm_q, &tm_k, a, n_qtiles, leader);
+    } else if (warp == kLoadWarpV) {
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV>(sm, &tm_q, &tm_v, a, n_qtiles, leader);
     } else if (warp == kMmaWarp) {
       mma_role(sm, tmem, a, n_qtiles, leader);
     }
     __syncwarp();
   } else {
-    if constexpr (RegSplit<FP8>::kSoftmax != 168) regs_increase<RegSplit<FP8>::kSoftmax>();
+    regs_increase<RegSplit<FP8>::kSoftmax>();
     softmax_role(sm, tmem, a, n_qtiles, warp, lane);
     __syncwarp();
   }
@@ -776,7 +807,11 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
 }  // namespace zyfa
 
 #ifdef ZYFA_TRACE
+// Copies the trace out and clears it for the next launch.
 extern "C" int zyfa_trace_read(void* dst, size_t bytes) {
-  return cudaMemcpyFromSymbol(dst, zyfa::zyfa_trace_buf, bytes) == cudaSuccess ? 0 : 3;
+  if (cudaMemcpyFromSymbol(dst, zyfa::zyfa_trace_buf, bytes) != cudaSuccess) return 3;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, zyfa::zyfa_trace_buf) != cudaSuccess) return 3;
+  return cudaMemset(p, 0, sizeof(zyfa::zyfa_trace_buf)) == cudaSuccess ? 0 : 3;
 }
 #endif
