@@ -186,8 +186,30 @@ int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t
     return fail(ZYFA_ERR_INVALID_ARG, "grid too large");
   DeviceInfo* d;
   if (int r = device_info(&d)) return r;
-  zyfa::QuantArgs a{x, stride_b, stride_s, stride_h, static_cast<uint8_t*>(out), scales, B, S, H, D, hadamard};
-  cudaError_t e = zyfa::launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+  zyfa::QuantArgs a{x, stride_b, stride_s, stride_h, static_cast<uint8_t*>(out), scales, B, S, H, D, hadamard,
+                    d->status, g_timeout_ns, d->sm_count};
+  cudaError_t e;
+  // TMA streaming kernel when the input allows 16-byte tiled copies; the
+  // register kernel otherwise. Both produce the same bytes.
+  const bool tma_ok = aligned(x, 16) && aligned(out, 16) && stride_b % 8 == 0 && stride_s % 8 == 0 &&
+                      stride_h % 8 == 0 && stride_b < (int64_t(1) << 38) && stride_s < (int64_t(1) << 38) &&
+                      stride_h < (int64_t(1) << 38);
+  if (tma_ok) {
+    CUtensorMap tm;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(stride_h) * 2, static_cast<cuuint64_t>(stride_s) * 2,
+                                    static_cast<cuuint64_t>(stride_b) * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1u, 128u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult cr = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, gstrides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(x) failed: %d", (int)cr);
+    e = zyfa::launch_quantize_fp8_stream(tm, a, static_cast<cudaStream_t>(stream));
+  } else {
+    e = zyfa::launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8 launch");
   return ZYFA_OK;
 }

@@ -18,9 +18,17 @@ struct QuantArgs {
   float* scales;          // [B,H,ceil(S/128)]
   int B, S, H, D;
   int hadamard;
+  unsigned int* status;   // device status word (streaming kernel's bounded waits)
+  uint64_t timeout_ns;
+  int num_sms;
 };
 
+// Register kernel: any 4-byte aligned input with even strides.
 cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
+// Streaming kernel: persistent CTAs, TMA ring of input blocks. tm_x is a 4-D
+// map (D, H, S, B) over x, no swizzle, box D x 1 x 128 x 1 (needs a 16-byte
+// aligned base and strides that are multiples of 8 elements).
+cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
   int B, S, Hq, Hkv, Dqk, Dv;

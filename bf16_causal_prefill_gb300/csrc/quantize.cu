@@ -33,6 +33,22 @@ constexpr float kInvSqrt128 = 0.0883883476483184405501055452631f;   // RN to fp3
 constexpr float kE4m3Max = 448.0f;
 constexpr float kZeroGuard = 1e-8f;
 
+// y / scale rounded to fp32, for a whole block with one scale: Markstein's
+// correction step (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// rinv = RN(1/scale) and the faithful q0 = RN(y * rinv), the remainder
+// rem = y - scale * q0 is exact under FMA and RN(q0 + rem * rinv) is the
+// correctly rounded quotient whenever no intermediate underflows. Every
+// quotient that can round to a nonzero e4m3 code (|q| >= 2^-10, so y, scale
+// and rem are normal) is therefore exact; smaller ones round to a signed zero
+// code either way. A nonzero quotient has the sign of y; the sign is copied
+// from y so that y = -0 keeps it (the corrected sum would give +0).
+__device__ __forceinline__ float div_by_scale(float y, float scale, float rinv) {
+  const float q0 = __fmul_rn(y, rinv);
+  const float rem = __fmaf_rn(-scale, q0, y);
+  return copysignf(__fmaf_rn(rem, rinv, q0), y);
+}
+
 template <int D, bool kHadamard>
 __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(QuantArgs a) {
   constexpr int kPairs = D / 64;   // bf16 pairs per lane per row
@@ -101,6 +117,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(QuantArgs a
 #pragma unroll
   for (int w = 1; w < kQuantThreads / 32; ++w) bmax = fmaxf(bmax, red[w]);
   const float scale = (bmax < kZeroGuard) ? 1.0f : __fdiv_rn(bmax, kE4m3Max);
+  const float rinv = __frcp_rn(scale);
   if (threadIdx.x == 0) a.scales[(static_cast<int64_t>(b) * a.H + h) * nblk + blk] = scale;
 
 #pragma unroll
@@ -110,9 +127,162 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(QuantArgs a
     uint8_t* orow = a.out + ((static_cast<int64_t>(b) * a.S + s) * a.H + h) * D;
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
-      const float q0 = __fdiv_rn(v[rr][2 * i], scale);
-      const float q1 = __fdiv_rn(v[rr][2 * i + 1], scale);
+      const float q0 = div_by_scale(v[rr][2 * i], scale, rinv);
+      const float q1 = div_by_scale(v[rr][2 * i + 1], scale, rinv);
       *reinterpret_cast<uint16_t*>(orow + 2 * (lane + 32 * i)) = pack_e4m3x2(q0, q1);
+    }
+  }
+}
+
+// Streaming variant: one persistent CTA of 512 threads per SM walks the
+// (batch, head, block) list; a TMA ring of kStages input blocks keeps several
+// blocks in flight per SM while the current one is reduced and converted.
+// Warp w owns rows 8w..8w+7 of a block; lane l holds elements
+// kEl*l .. kEl*l+kEl-1 of a row (kEl = D/32), so shared-memory reads and the
+// code stores are contiguous per warp. With the rotation (D = 128) the
+// butterflies of span 1 and 2 are in-lane and spans 4..64 are lane shuffles
+// (xor 1..16), in the same order and rounding as the register kernel.
+constexpr int kStreamThreads = 512;
+constexpr int kStreamRowsPerWarp = kBlockTokens / (kStreamThreads / 32);   // 8
+constexpr unsigned int kStatusQuantTimeout = 0x8u;
+
+template <int D>
+struct StreamCfg {
+  static constexpr int kStages = D == 128 ? 4 : 3;
+  static constexpr int kBlockBytes = kBlockTokens * D * 2;
+  static constexpr int kSmemBytes = kStages * kBlockBytes + 1024;
+};
+
+template <int D, bool kHadamard>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    quantize_fp8_stream_kernel(const __grid_constant__ CUtensorMap tm_x, QuantArgs a) {
+  using SC = StreamCfg<D>;
+  constexpr int kEl = D / 32;
+  static_assert(!kHadamard || D == 128, "rotation is defined for head dim 128");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* buf = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ __align__(8) uint64_t full[SC::kStages];
+  __shared__ float red[2][kStreamThreads / 32];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
+  const long long total = static_cast<long long>(a.B) * a.H * nblk;
+  const long long first = blockIdx.x, step = gridDim.x;
+
+  auto coords = [&](long long g, int& b, int& h, int& blk) {
+    blk = static_cast<int>(g % nblk);
+    const long long bh = g / nblk;
+    h = static_cast<int>(bh % a.H);
+    b = static_cast<int>(bh / a.H);
+  };
+  auto issue = [&](long long g, int st) {
+    int b, h, blk;
+    coords(g, b, h, blk);
+    mbar_arrive_expect_tx(&full[st], SC::kBlockBytes);
+    tma_load_4d(buf + st * SC::kBlockBytes, &tm_x, &full[st], 0, h, blk * kBlockTokens, b);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SC::kStages; ++i) mbar_init(&full[i], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SC::kStages; ++i)
+      if (first + i * step < total) issue(first + i * step, i);
+  }
+
+  int it = 0;
+  for (long long g = first; g < total; g += step, ++it) {
+    const int st = it % SC::kStages;
+    const uint32_t par = static_cast<uint32_t>(it / SC::kStages) & 1u;
+    int b, h, blk;
+    coords(g, b, h, blk);
+    const bool ok = mbar_wait(&full[st], par, &abort_flag, a.status, kStatusQuantTimeout, a.timeout_ns);
+
+    float v[kStreamRowsPerWarp][kEl];
+    float amax = 0.f;
+    if (ok) {
+      const uint8_t* tile = buf + st * SC::kBlockBytes;
+#pragma unroll
+      for (int rr = 0; rr < kStreamRowsPerWarp; ++rr) {
+        const int r = warp * kStreamRowsPerWarp + rr;
+        const __nv_bfloat162* src =
+            reinterpret_cast<const __nv_bfloat162*>(tile + (r * D + kEl * lane) * 2);
+#pragma unroll
+        for (int e = 0; e < kEl / 2; ++e) {
+          const float2 f = __bfloat1622float2(src[e]);
+          v[rr][2 * e] = f.x;
+          v[rr][2 * e + 1] = f.y;
+        }
+        if constexpr (kHadamard) {
+          // spans 1 and 2 inside the lane's four elements
+#pragma unroll
+          for (int hs = 1; hs <= 2; hs <<= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (e & hs) continue;
+              const float a0 = v[rr][e], a1 = v[rr][e + hs];
+              v[rr][e] = __fadd_rn(a0, a1);
+              v[rr][e + hs] = __fsub_rn(a0, a1);
+            }
+          }
+          // spans 4..64: partner lane differs in bit log2(span) - 2
+#pragma unroll
+          for (int m = 1; m <= 16; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float o = __shfl_xor_sync(0xffffffffu, v[rr][e], m);
+              v[rr][e] = upper ? __fsub_rn(o, v[rr][e]) : __fadd_rn(v[rr][e], o);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[rr][e] = __fmul_rn(v[rr][e], kInvSqrt128);
+        }
+#pragma unroll
+        for (int e = 0; e < kEl; e += 2) amax = max3f(amax, fabsf(v[rr][e]), fabsf(v[rr][e + 1]));
+      }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    if (lane == 0) red[it & 1][warp] = amax;
+    // Every thread has its rows in registers: the stage may be refilled.
+    if (__syncthreads_or(!ok)) break;
+    if (threadIdx.x == 0 && g + SC::kStages * step < total) issue(g + SC::kStages * step, st);
+    float bmax = red[it & 1][0];
+#pragma unroll
+    for (int w = 1; w < kStreamThreads / 32; ++w) bmax = fmaxf(bmax, red[it & 1][w]);
+    const float scale = (bmax < kZeroGuard) ? 1.0f : __fdiv_rn(bmax, kE4m3Max);
+    const float rinv = __frcp_rn(scale);
+    if (threadIdx.x == 0) a.scales[(static_cast<int64_t>(b) * a.H + h) * nblk + blk] = scale;
+#pragma unroll
+    for (int rr = 0; rr < kStreamRowsPerWarp; ++rr) {
+      const int s = blk * kBlockTokens + warp * kStreamRowsPerWarp + rr;
+      if (s >= a.S) break;
+      uint8_t* orow = a.out + ((static_cast<int64_t>(b) * a.S + s) * a.H + h) * D + kEl * lane;
+      if constexpr (kEl == 4) {
+        const uint32_t lo = pack_e4m3x2(div_by_scale(v[rr][0], scale, rinv), div_by_scale(v[rr][1], scale, rinv));
+        const uint32_t hi = pack_e4m3x2(div_by_scale(v[rr][2], scale, rinv), div_by_scale(v[rr][3], scale, rinv));
+        *reinterpret_cast<uint32_t*>(orow) = lo | (hi << 16);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kEl / 2; ++e)
+          *reinterpret_cast<uint16_t*>(orow + 2 * e) =
+              pack_e4m3x2(div_by_scale(v[rr][2 * e], scale, rinv), div_by_scale(v[rr][2 * e + 1], scale, rinv));
+      }
+    }
+  }
+  // On abort, let every issued copy land before the CTA exits (bounded).
+  if (threadIdx.x == 0 && abort_flag) {
+    int k = 0;
+    for (long long g = first; g < total && k < it + SC::kStages; g += step, ++k) {
+      if (k < it) continue;
+      const int st = k % SC::kStages;
+      if (!mbar_wait_drain(&full[st], static_cast<uint32_t>(k / SC::kStages) & 1u, 200000000ull))
+        atomicOr(a.status, 0x100u);
     }
   }
 }
@@ -132,6 +302,24 @@ cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <int D, bool H>
+static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream) {
+  auto kern = quantize_fp8_stream_kernel<D, H>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long total = static_cast<long long>(a.B) * a.H * ((a.S + kBlockTokens - 1) / kBlockTokens);
+  const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
+  kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream) {
+  if (a.D == 128 && a.hadamard) return launch_stream<128, true>(tm_x, a, stream);
+  if (a.D == 128) return launch_stream<128, false>(tm_x, a, stream);
+  if (a.D == 192) return launch_stream<192, false>(tm_x, a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace zyfa

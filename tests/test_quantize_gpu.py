@@ -84,3 +84,15 @@ def test_workload_tensors(name):
     q, k, v = workloads.make_qkv(w)
     for t, had in ((q, False), (q, True), (k, True), (v, False)):
         _check(t, had)
+
+
+@pytest.mark.parametrize("D,had", [(128, False), (128, True), (192, False)])
+def test_unaligned_views_use_the_register_kernel(D, had):
+    """Views whose base or strides do not allow 16-byte tiled copies go to the
+    register kernel; contiguous tensors go to the streaming (TMA) kernel. Both
+    must give the oracle's bytes."""
+    g = torch.Generator().manual_seed(D + had)
+    big = (torch.randn(2, 300, 3, D + 4, generator=g) * 2).to(torch.bfloat16)
+    x_cpu = big[..., 2:2 + D].contiguous()
+    _check(x_cpu, had, big.cuda()[..., 2:2 + D])      # stride_h = D + 4, base offset 4 bytes
+    _check(x_cpu, had)                                # contiguous copy: streaming kernel
