@@ -137,11 +137,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(QuantArgs a
 // Streaming variant: one persistent CTA of 512 threads per SM walks the
 // (batch, head, block) list; a TMA ring of kStages input blocks keeps several
 // blocks in flight per SM while the current one is reduced and converted.
-// Warp w owns rows 8w..8w+7 of a block; lane l holds elements
-// kEl*l .. kEl*l+kEl-1 of a row (kEl = D/32), so shared-memory reads and the
-// code stores are contiguous per warp. With the rotation (D = 128) the
-// butterflies of span 1 and 2 are in-lane and spans 4..64 are lane shuffles
-// (xor 1..16), in the same order and rounding as the register kernel.
+// Eight lanes share a row (a warp holds four rows at a time, two such row
+// groups per warp): lane j of a row holds the 8-element groups starting at
+// 8j, 64 + 8j (and 128 + 8j at D = 192), read as 16-byte shared-memory loads
+// that cover 128 contiguous bytes per row. With the rotation (D = 128) the
+// butterflies of span 1, 2, 4 (inside a group) and 64 (between the lane's two
+// groups) are in registers and spans 8, 16, 32 are shuffles over the row's
+// eight lanes; each butterfly is one rounded add or subtract, applied in the
+// order 1, 2, ..., 64 as in the register kernel.
 constexpr int kStreamThreads = 512;
 constexpr int kStreamRowsPerWarp = kBlockTokens / (kStreamThreads / 32);   // 8
 constexpr unsigned int kStatusQuantTimeout = 0x8u;
@@ -157,7 +160,7 @@ template <int D, bool kHadamard>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     quantize_fp8_stream_kernel(const __grid_constant__ CUtensorMap tm_x, QuantArgs a) {
   using SC = StreamCfg<D>;
-  constexpr int kEl = D / 32;
+  constexpr int kGroups = D / 64;   // 8-element groups per lane and row
   static_assert(!kHadamard || D == 128, "rotation is defined for head dim 128");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* buf = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -202,48 +205,59 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     coords(g, b, h, blk);
     const bool ok = mbar_wait(&full[st], par, &abort_flag, a.status, kStatusQuantTimeout, a.timeout_ns);
 
-    float v[kStreamRowsPerWarp][kEl];
+    // v[g][k*8 + e]: row warp*8 + 4*g + lane/8, element 64*k + 8*(lane%8) + e
+    float v[2][kGroups * 8];
     float amax = 0.f;
     if (ok) {
       const uint8_t* tile = buf + st * SC::kBlockBytes;
 #pragma unroll
-      for (int rr = 0; rr < kStreamRowsPerWarp; ++rr) {
-        const int r = warp * kStreamRowsPerWarp + rr;
-        const __nv_bfloat162* src =
-            reinterpret_cast<const __nv_bfloat162*>(tile + (r * D + kEl * lane) * 2);
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int r = warp * kStreamRowsPerWarp + 4 * g2 + (lane >> 3);
 #pragma unroll
-        for (int e = 0; e < kEl / 2; ++e) {
-          const float2 f = __bfloat1622float2(src[e]);
-          v[rr][2 * e] = f.x;
-          v[rr][2 * e + 1] = f.y;
+        for (int k = 0; k < kGroups; ++k) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(tile + (r * D + 64 * k + 8 * (lane & 7)) * 2);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            v[g2][8 * k + 2 * e] = f.x;
+            v[g2][8 * k + 2 * e + 1] = f.y;
+          }
         }
         if constexpr (kHadamard) {
-          // spans 1 and 2 inside the lane's four elements
+          // spans 1, 2, 4 inside each group of eight
 #pragma unroll
-          for (int hs = 1; hs <= 2; hs <<= 1) {
+          for (int hs = 1; hs <= 4; hs <<= 1) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 16; ++e) {
               if (e & hs) continue;
-              const float a0 = v[rr][e], a1 = v[rr][e + hs];
-              v[rr][e] = __fadd_rn(a0, a1);
-              v[rr][e + hs] = __fsub_rn(a0, a1);
+              const float a0 = v[g2][e], a1 = v[g2][e + hs];
+              v[g2][e] = __fadd_rn(a0, a1);
+              v[g2][e + hs] = __fsub_rn(a0, a1);
             }
           }
-          // spans 4..64: partner lane differs in bit log2(span) - 2
+          // spans 8, 16, 32: partner lane differs in bit 0, 1, 2 of the row lane
 #pragma unroll
-          for (int m = 1; m <= 16; m <<= 1) {
-            const bool upper = (lane & m) != 0;
+          for (int m = 1; m <= 4; m <<= 1) {
+            const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float o = __shfl_xor_sync(0xffffffffu, v[rr][e], m);
-              v[rr][e] = upper ? __fsub_rn(o, v[rr][e]) : __fadd_rn(v[rr][e], o);
+            for (int e = 0; e < 16; ++e) {
+              const float o = __shfl_xor_sync(0xffffffffu, v[g2][e], m);
+              v[g2][e] = __fmaf_rn(sgn, v[g2][e], o);   // lower: o + v, upper: o - v
             }
           }
+          // span 64: the lane's two groups
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[rr][e] = __fmul_rn(v[rr][e], kInvSqrt128);
+          for (int e = 0; e < 8; ++e) {
+            const float a0 = v[g2][e], a1 = v[g2][8 + e];
+            v[g2][e] = __fadd_rn(a0, a1);
+            v[g2][8 + e] = __fsub_rn(a0, a1);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[g2][e] = __fmul_rn(v[g2][e], kInvSqrt128);
         }
 #pragma unroll
-        for (int e = 0; e < kEl; e += 2) amax = max3f(amax, fabsf(v[rr][e]), fabsf(v[rr][e + 1]));
+        for (int e = 0; e < kGroups * 8; e += 2) amax = max3f(amax, fabsf(v[g2][e]), fabsf(v[g2][e + 1]));
       }
     }
 #pragma unroll
@@ -259,19 +273,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const float rinv = __frcp_rn(scale);
     if (threadIdx.x == 0) a.scales[(static_cast<int64_t>(b) * a.H + h) * nblk + blk] = scale;
 #pragma unroll
-    for (int rr = 0; rr < kStreamRowsPerWarp; ++rr) {
-      const int s = blk * kBlockTokens + warp * kStreamRowsPerWarp + rr;
-      if (s >= a.S) break;
-      uint8_t* orow = a.out + ((static_cast<int64_t>(b) * a.S + s) * a.H + h) * D + kEl * lane;
-      if constexpr (kEl == 4) {
-        const uint32_t lo = pack_e4m3x2(div_by_scale(v[rr][0], scale, rinv), div_by_scale(v[rr][1], scale, rinv));
-        const uint32_t hi = pack_e4m3x2(div_by_scale(v[rr][2], scale, rinv), div_by_scale(v[rr][3], scale, rinv));
-        *reinterpret_cast<uint32_t*>(orow) = lo | (hi << 16);
-      } else {
+    for (int g2 = 0; g2 < 2; ++g2) {
+      const int s = blk * kBlockTokens + warp * kStreamRowsPerWarp + 4 * g2 + (lane >> 3);
+      if (s < a.S) {
+        uint8_t* orow = a.out + ((static_cast<int64_t>(b) * a.S + s) * a.H + h) * D + 8 * (lane & 7);
 #pragma unroll
-        for (int e = 0; e < kEl / 2; ++e)
-          *reinterpret_cast<uint16_t*>(orow + 2 * e) =
-              pack_e4m3x2(div_by_scale(v[rr][2 * e], scale, rinv), div_by_scale(v[rr][2 * e + 1], scale, rinv));
+        for (int k = 0; k < kGroups; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_e4m3x2(div_by_scale(v[g2][8 * k + 2 * e], scale, rinv),
+                               div_by_scale(v[g2][8 * k + 2 * e + 1], scale, rinv));
+          *reinterpret_cast<uint2*>(orow + 64 * k) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+        }
       }
     }
   }
