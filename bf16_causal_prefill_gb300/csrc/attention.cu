@@ -185,6 +185,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// Warp-wide bounded wait on two barriers at once (one poll loop, one vote):
+// each wait costs the MMA warp a fixed overhead during which the tensor pipe
+// drains, so the two TMA barriers of an iteration share one.
+__device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64_t* bar2, uint32_t par2,
+                                           volatile int* abort_flag, unsigned int* status, unsigned int code,
+                                           uint64_t timeout_ns) {
+  bool ok1 = mbar_try_wait(bar1, par1), ok2 = mbar_try_wait(bar2, par2);
+  if (!(ok1 && ok2)) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (!ok1) ok1 = mbar_try_wait(bar1, par1);
+      if (!ok2) ok2 = mbar_try_wait(bar2, par2);
+      if (ok1 && ok2) break;
+      if (*abort_flag) break;
+      if ((it & 63u) == 0 && global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, code);
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok1 && ok2);
+}
+
 // ------------------------------------------------------------------ loader --
 // Two loader warps: one streams Q and K, the other V. A thread's TMA copies
 // are processed one after another (one 16 KB tile takes ~430 cycles however
@@ -360,11 +384,12 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       for (int j = 0; j < w.n_kv; ++j) {
         const bool need_k = (j + 1 < w.n_kv);      // K_{j+1} feeds S_A(j+1) and/or S_B(j+1)
         if (leader) ZTRACE(2, tix, 10);
-        ZYFA_WAIT(sm.v_full(vs), vph);
-        if (leader) ZTRACE(2, tix, 24);
         if (need_k) {
-          ZYFA_WAIT(sm.k_full(ks), kph);
-          if (leader) ZTRACE(2, tix, 25);
+          if (!(ok = warp_wait2(sm.v_full(vs), vph, sm.k_full(ks), kph, abort_flag, a.status, kStatusMmaTimeout,
+                                a.timeout_ns)))
+            break;
+        } else {
+          ZYFA_WAIT(sm.v_full(vs), vph);
         }
         if (leader) ZTRACE(2, tix, 11);
         if (j < w.n_a) {
