@@ -17,6 +17,7 @@ attention on the same quantised inputs).
 """
 from __future__ import annotations
 
+import math
 from typing import Iterable, Optional
 
 import numpy as np
@@ -73,6 +74,44 @@ def causal_attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: fl
         s = s - np.max(s)
         p = np.exp(s)
         res.append((p / np.sum(p)) @ vv)
+    return np.stack(res)
+
+
+def causal_attention_rows_pquant(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                                 b: int, h: int, rows: Iterable[int], block: int = 64) -> np.ndarray:
+    """Selected output rows with the probabilities quantised the way the ZYFA
+    post describes ("Per-Block Scaling and Normalization by the Rounded Row
+    Sum"): the row's probabilities p (max-subtracted, as in the exact oracle)
+    are cut into blocks of `block` keys; each block is multiplied by 2^kb with
+    kb = floor(-log2(block max)), so its largest value lies in (0.5, 1]; the
+    products are rounded to e4m3 (nearest, ties to even); the power of two is
+    divided back out, giving weights W; the output is sum(W v) / sum(W), i.e.
+    normalised by the sum of the rounded weights. A block whose probabilities
+    all underflow to zero contributes nothing. Used only for the error-by-stage
+    report (P-rounding error as the pages define it), not as a parity gate.
+    Returns [len(rows), Dv] float64."""
+    from . import fp8 as _fp8
+
+    Hq = q.shape[2]
+    Hkv = k.shape[2]
+    g = kv_head(h, Hq, Hkv)
+    res = []
+    for i in rows:
+        qi = np.asarray(q[b, i, h, :], dtype=np.float64)
+        kk = np.asarray(k[b, : i + 1, g, :], dtype=np.float64)
+        vv = np.asarray(v[b, : i + 1, g, :], dtype=np.float64)
+        s = (kk @ qi) * scale
+        p = np.exp(s - np.max(s))
+        w = np.zeros_like(p)
+        for c in range(0, p.size, block):
+            pb = p[c:c + block]
+            mb = float(np.max(pb))
+            if mb <= 0.0:
+                continue
+            kb = math.floor(-math.log2(mb))
+            codes = _fp8.e4m3_rne(np.ldexp(pb, kb))
+            w[c:c + block] = np.ldexp(_fp8.e4m3_decode(codes), -kb)
+        res.append((w @ vv) / np.sum(w))
     return np.stack(res)
 
 
