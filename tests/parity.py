@@ -73,6 +73,23 @@ def sampled_rows_oracle(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: floa
     return out
 
 
+def sampled_rows_pquant(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, rows: List[int]) -> np.ndarray:
+    """Like sampled_rows_oracle, with the probabilities quantised per 64-key
+    block as the pages describe (oracle.attention.causal_attention_rows_pquant)."""
+    B, S, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    out = np.empty((B, len(rows), Hq, v.shape[3]))
+    group = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            kk = np.asarray(k[b:b + 1, :, g:g + 1], np.float64)
+            vv = np.asarray(v[b:b + 1, :, g:g + 1], np.float64)
+            qq = np.asarray(q[b:b + 1, :, h:h + 1], np.float32)
+            out[b, :, h] = oattn.causal_attention_rows_pquant(qq, kk, vv, scale, 0, 0, rows)
+    return out
+
+
 def gpu_rows(o: torch.Tensor, rows: List[int], heads: Optional[List[int]] = None,
              batches: Optional[List[int]] = None) -> np.ndarray:
     B, S, Hq, _ = o.shape
