@@ -524,17 +524,15 @@ __device__ __forceinline__ uint32_t exp2_e4m3x4_sum(float2 x01, float2 x23, floa
 //   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the fp32 p.
 //   FP8:  e4m3 codes, four per word, into pk[8c .. 8c+7]; acc sums the
 //         rounded values.
-// mxa tracks the raw score maximum.
 template <bool FP8>
 __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, float cb, uint32_t* pk,
-                                            float2 (&acc)[2], float (&mxa)[2]) {
+                                            float2 (&acc)[2]) {
   const float2 a2 = make_float2(ca, ca);
   const float2 b2 = make_float2(cb, cb);
   if constexpr (!FP8) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float s0 = u2f(s[2 * i]), s1 = u2f(s[2 * i + 1]);
-      mxa[i & 1] = max3f(mxa[i & 1], s0, s1);
       const float2 x = __ffma2_rn(make_float2(s0, s1), a2, b2);
       const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
       pk[16 * c + i] = pack_bf16x2(p.x, p.y);
@@ -544,8 +542,6 @@ __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float s0 = u2f(s[4 * i]), s1 = u2f(s[4 * i + 1]), s2 = u2f(s[4 * i + 2]), s3 = u2f(s[4 * i + 3]);
-      mxa[0] = max3f(mxa[0], s0, s1);
-      mxa[1] = max3f(mxa[1], s2, s3);
       const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
       const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
 #ifdef ZYFA_EX2_F16
@@ -635,68 +631,80 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       const bool diag = (j == n - 1);
       uint32_t pk[kPk];
       float psum = 0.f;
-      bool first = (j == 0);
-      bool redone = false;
-      for (;;) {
+      const bool first = (j == 0);
+      if constexpr (FP8) {
+        // The whole row of S in one load and its maximum first: the offset is
+        // set (first tile) or moved (a tile whose largest P' would leave the
+        // window) before any exponential, so no tile computes them twice.
+        // Rows whose scores span many binades (activation-like inputs) move
+        // the offset on a large share of tiles; there this order is 1.5x
+        // faster than computing the exponentials speculatively and redoing
+        // them, for a few percent on rows that rarely move it.
         uint32_t s[128];
-        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float mxa[2] = {-INFINITY, -INFINITY};
-        if (first || FP8) {
-          // The whole row of S in one load: the first tile needs the maximum
-          // before any exponential; FP8 rows are short enough to hold it.
-          tmem_ld128(tS, s);
-          if (diag) {
+        tmem_ld128(tS, s);
+        if (diag) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
-          }
-          if (first) {
-            const float mx0 = row_max(s);
-            if constexpr (FP8) {
-              top = mx0 * cj + lsv;
-              m = top - kWinCentre;
-            } else {
-              m = mx0 * cj;
-            }
-          }
-          const float cb = FP8 ? (lsv - m) : -m;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) probs_chunk<FP8>(c, &s[32 * c], cj, cb, pk, acc, mxa);
+          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
+        }
+        const float bm = row_max(s) * cj + lsv;
+        bool moved = false;
+        float rho = 1.f;
+        if (first) {
+          top = bm;
+          m = top - kWinCentre;
         } else {
-          // BF16 later tiles: exponentials with the current offset, S read
-          // in 32-column chunks.
-          const float cb = -m;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
-            if (diag) mask_chunk(&s[32 * c], 32 * c, r);
-            probs_chunk<FP8>(c, &s[32 * c], cj, cb, pk, acc, mxa);
+          const float rel = bm - m;
+          const bool need = rel > kWinHi || (rel < kWinLo && bm > top - kFloorBinades);
+          const float m_new = need ? fmaxf(bm - kWinCentre, fmaxf(top, bm) - kFloorBinades) : m;
+          top = fmaxf(top, bm);
+          moved = __any_sync(0xffffffffu, need);
+          if (moved) {
+            rho = ex2_approx(m - m_new);
+            l *= rho;
+            m = m_new;
           }
         }
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) probs_chunk<true>(c, &s[32 * c], cj, lsv - m, pk, acc);
         const float2 t = __fadd2_rn(acc[0], acc[1]);
         psum = t.x + t.y;
-        if (first || redone) break;
-        // Check the offset against this tile's maximum; redo the (rare) rows
-        // that need a new one. S is intact: P has not been written yet.
-        const float mx = fmaxf(mxa[0], mxa[1]);
-        bool need;
-        float m_new;
-        if constexpr (FP8) {
-          const float bm = mx * cj + lsv;
-          const float rel = bm - m;
-          need = rel > kWinHi || (rel < kWinLo && bm > top - kFloorBinades);
-          m_new = need ? fmaxf(bm - kWinCentre, fmaxf(top, bm) - kFloorBinades) : m;
-          top = fmaxf(top, bm);
-        } else {
-          const float xmax = mx * cj;
-          need = xmax > m + kRescaleThreshold;
-          m_new = need ? xmax : m;
+        // O is final for the previous tiles (their PV completed before this
+        // S); rescaling it after the exponentials keeps S out of registers.
+        if (moved) rescale_o_row(tO, rho);
+      } else {
+        // The whole row of S in one load and its maximum first. The first
+        // tile sets the running maximum; later tiles keep it stale while
+        // their own stays within 2^8 of it, otherwise move it before the
+        // exponentials (O is rescaled after them). No tile computes its
+        // exponentials twice.
+        uint32_t s[128];
+        tmem_ld128(tS, s);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
         }
-        if (!__any_sync(0xffffffffu, need)) break;
-        const float rho = ex2_approx(m - m_new);
-        l *= rho;
-        m = m_new;
-        rescale_o_row(tO, rho);
-        redone = true;
+        const float xmax = row_max(s) * cj;
+        bool moved = false;
+        float rho = 1.f;
+        if (first) {
+          m = xmax;
+        } else {
+          const bool need = xmax > m + kRescaleThreshold;
+          moved = __any_sync(0xffffffffu, need);
+          if (moved) {
+            const float m_new = need ? xmax : m;
+            rho = ex2_approx(m - m_new);
+            l *= rho;
+            m = m_new;
+          }
+        }
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) probs_chunk<false>(c, &s[32 * c], cj, -m, pk, acc);
+        const float2 t = __fadd2_rn(acc[0], acc[1]);
+        psum = t.x + t.y;
+        if (moved) rescale_o_row(tO, rho);
       }
       if (tr) ZTRACE(wg, tix, 3);
       if constexpr (FP8) l = fmaf(psum, inv_sv, l);
