@@ -65,6 +65,14 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8.restype = c_int
     L.zyfa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
                                     c_float, vp, vp, vp, vp, vp]
+    L.zyfa_quantize_fp8_varlen.restype = c_int
+    L.zyfa_quantize_fp8_varlen.argtypes = [vp, i64, i64, vp, vp, vp, c_int, c_int, c_int, c_int, vp]
+    L.zyfa_attn_fwd_bf16_varlen.restype = c_int
+    L.zyfa_attn_fwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float,
+                                            vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_fp8_varlen.restype = c_int
+    L.zyfa_attn_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                           c_float, vp, vp, vp, vp, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     L.zyfa_set_debug.restype = c_int
@@ -177,6 +185,116 @@ def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: boo
     k8, ks = quantize_fp8(k, hadamard, stream=stream)
     v8, vs = quantize_fp8(v, False, stream=stream)
     o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream)
+    return o, (q8, qs, k8, ks, v8, vs)
+
+
+# ------------------------------------------------------ packed varlen batches
+def _cu_host(cu_seqlens) -> Tuple[ctypes.Array, int, int]:
+    """Host int32 copy of cu_seqlens (list, numpy array or tensor; a CUDA
+    tensor is copied to the host, which synchronises). Returns the ctypes
+    array, B and the longest sequence."""
+    if isinstance(cu_seqlens, torch.Tensor):
+        vals = [int(x) for x in cu_seqlens.detach().to("cpu", torch.int64).tolist()]
+    else:
+        vals = [int(x) for x in cu_seqlens]
+    if len(vals) < 2:
+        raise ValueError("cu_seqlens needs at least two entries")
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    max_len = max(vals[i + 1] - vals[i] for i in range(len(vals) - 1))
+    return arr, len(vals) - 1, max_len
+
+
+def _require_packed(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError(f"{name} must be 3-D [T,H,D] with a contiguous last dim")
+
+
+def _i64x2(a: int, b: int):
+    return (ctypes.c_int64 * 2)(a, b)
+
+
+def _strides2(t: torch.Tensor):
+    return _i64x2(t.stride(0), t.stride(1))
+
+
+def quantize_fp8_varlen(x: torch.Tensor, cu_seqlens, hadamard: bool = False,
+                        stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-(sequence, head, 128-token block) e4m3 quantisation of a packed bf16
+    [T,H,D] tensor. Returns (codes uint8 [T,H,D], scales float32
+    [B,H,ceil(max_len/128)])."""
+    _require_packed(x, "x", torch.bfloat16)
+    T, H, D = x.shape
+    cu, B, max_len = _cu_host(cu_seqlens)
+    out = torch.empty((T, H, D), dtype=torch.uint8, device=x.device)
+    scales = torch.zeros((B, H, scale_blocks(max_len)), dtype=torch.float32, device=x.device)
+    _check(lib().zyfa_quantize_fp8_varlen(x.data_ptr(), x.stride(0), x.stride(1), out.data_ptr(), scales.data_ptr(),
+                                          cu, B, H, D, int(bool(hadamard)), _stream_ptr(x, stream)))
+    return out, scales
+
+
+def attn_fwd_bf16_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens,
+                         softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Causal attention over a packed variable-length batch: q [T,Hq,Dqk],
+    k [T,Hkv,Dqk], v [T,Hkv,Dv] -> o [T,Hq,Dv] bf16; each sequence attends to
+    itself only."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require_packed(t, n, torch.bfloat16)
+    T, Hq, Dqk = q.shape
+    Hkv, Dv = k.shape[1], v.shape[2]
+    cu, B, _ = _cu_host(cu_seqlens)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_bf16_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), cu, B, Hq,
+                                           Hkv, Dqk, Dv, float(softmax_scale), _strides2(q), _strides2(k),
+                                           _strides2(v), _strides2(out), _stream_ptr(q, stream)))
+    return out
+
+
+def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor,
+                        v8: torch.Tensor, v_scale: torch.Tensor, cu_seqlens, softmax_scale: Optional[float] = None,
+                        out: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """FP8 causal attention over a packed variable-length batch (codes and
+    scales as written by quantize_fp8_varlen) -> bf16 o [T,Hq,Dv]."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _require_packed(t, n, torch.uint8)
+    T, Hq, Dqk = q8.shape
+    Hkv, Dv = k8.shape[1], v8.shape[2]
+    cu, B, max_len = _cu_host(cu_seqlens)
+    nb = scale_blocks(max_len)
+    for t, n, h in ((q_scale, "q_scale", Hq), (k_scale, "k_scale", Hkv), (v_scale, "v_scale", Hkv)):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, h, nb):
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor [B, H, ceil(max_len/128)]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_fp8_varlen(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                          v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, B, Hq, Hkv, Dqk,
+                                          Dv, float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
+                                          _strides2(out), _stream_ptr(q8, stream)))
+    return out
+
+
+def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens, hadamard: bool = False,
+                       softmax_scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None):
+    """The FP8 prefill path over a packed variable-length batch. Returns
+    (o, (q8, qs, k8, ks, v8, vs))."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[2])
+    q8, qs = quantize_fp8_varlen(q, cu_seqlens, hadamard, stream=stream)
+    k8, ks = quantize_fp8_varlen(k, cu_seqlens, hadamard, stream=stream)
+    v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream)
+    o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream)
     return o, (q8, qs, k8, ks, v8, vs)
 
 

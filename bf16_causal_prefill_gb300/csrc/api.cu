@@ -3,11 +3,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/zyfa.h"
 #include "internal.h"
@@ -234,7 +236,7 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
   if ((r = make_map(&tq, q, dt, elt, Dqk, Hq, S, B, qs, "q")) || (r = make_map(&tk, k, dt, elt, Dqk, Hkv, S, B, ks, "k")) ||
       (r = make_map(&tv, v, dt, elt, Dv, Hkv, S, B, vs, "v")))
     return r;
-  zyfa::AttnArgs a;
+  zyfa::AttnArgs a{};
   a.B = B; a.S = S; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.o = o; a.o_sb = os[0]; a.o_ss = os[1]; a.o_sh = os[2];
@@ -243,6 +245,7 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
   a.timeout_ns = g_timeout_ns;
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
+  a.scale_blocks = (S + 127) / 128;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
@@ -262,6 +265,152 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
                       const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
   return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream);
+}
+
+// ----------------------------------------------------- packed varlen batches
+// Host cu_seqlens: B + 1 nondecreasing offsets starting at 0.
+static int read_seqlens(const int32_t* cu, int B, int* total, int* max_len) {
+  if (!cu) return fail(ZYFA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (B < 1 || B > zyfa::kMaxVarlenSeqs)
+    return fail(ZYFA_ERR_INVALID_ARG, "batch %d outside 1..%d", B, zyfa::kMaxVarlenSeqs);
+  if (cu[0] != 0) return fail(ZYFA_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+  int mx = 0;
+  for (int i = 0; i < B; ++i) {
+    if (cu[i + 1] < cu[i]) return fail(ZYFA_ERR_INVALID_ARG, "cu_seqlens must be nondecreasing (at %d)", i);
+    mx = std::max(mx, cu[i + 1] - cu[i]);
+  }
+  if (mx > 2 * 128 * zyfa::kMaxVarlenLevels)
+    return fail(ZYFA_ERR_UNSUPPORTED, "sequence of %d tokens exceeds %d", mx, 2 * 128 * zyfa::kMaxVarlenLevels);
+  *total = cu[B];
+  *max_len = mx;
+  return ZYFA_OK;
+}
+
+static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
+                       const float* vsc, void* o, const int32_t* cu, int B, int Hq, int Hkv, int Dqk, int Dv,
+                       float softmax_scale, const int64_t qs[2], const int64_t ks[2], const int64_t vs[2],
+                       const int64_t os[2], void* stream) {
+  int T = 0, max_len = 0;
+  if (int r = read_seqlens(cu, B, &T, &max_len)) return r;
+  if (!qs || !ks || !vs || !os) return fail(ZYFA_ERR_INVALID_ARG, "strides pointer is null");
+  if (T == 0) return ZYFA_OK;   // nothing to compute
+  // The packed tensors as one batch of T tokens.
+  const int64_t q3[3] = {qs[0] * T, qs[0], qs[1]}, k3[3] = {ks[0] * T, ks[0], ks[1]};
+  const int64_t v3[3] = {vs[0] * T, vs[0], vs[1]}, o3[3] = {os[0] * T, os[0], os[1]};
+  AttnCommon c{1, T, Hq, Hkv, Dqk, Dv, softmax_scale};
+  const int elt = fp8 ? 1 : 2;
+  if (int r = validate_attn(c, q, k, v, o, 16 / elt, q3, k3, v3, o3)) return r;
+  if (fp8) {
+    if (!qsc || !ksc || !vsc) return fail(ZYFA_ERR_INVALID_ARG, "null scale pointer");
+    if (!aligned(qsc, 4) || !aligned(ksc, 4) || !aligned(vsc, 4))
+      return fail(ZYFA_ERR_INVALID_ARG, "scale pointers must be 4-byte aligned");
+  }
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tq, tk, tv;
+  int r;
+  if ((r = make_map(&tq, q, dt, elt, Dqk, Hq, T, 1, q3, "q")) || (r = make_map(&tk, k, dt, elt, Dqk, Hkv, T, 1, k3, "k")) ||
+      (r = make_map(&tv, v, dt, elt, Dv, Hkv, T, 1, v3, "v")))
+    return r;
+  // Unit table: non-empty sequences, longest first; level k holds pair
+  // t = n_levels - 1 - k of every sequence with more than t pairs.
+  static thread_local zyfa::SeqTable tab;
+  std::vector<int> order;
+  for (int i = 0; i < B; ++i)
+    if (cu[i + 1] > cu[i]) order.push_back(i);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int x, int y) { return (cu[x + 1] - cu[x]) > (cu[y + 1] - cu[y]); });
+  tab.n_seqs = static_cast<int>(order.size());
+  for (int i = 0; i < tab.n_seqs; ++i) {
+    tab.start[i] = cu[order[i]];
+    tab.len[i] = cu[order[i] + 1] - cu[order[i]];
+    tab.index[i] = order[i];
+  }
+  auto pairs = [](int len) { return ((len + 127) / 128 + 1) / 2; };
+  tab.n_levels = pairs(max_len);
+  // cnt[t]: sequences with more than t pairs (a prefix of the sorted order)
+  std::vector<int> cnt(tab.n_levels);
+  int with = tab.n_seqs;
+  for (int t = 0; t < tab.n_levels; ++t) {
+    while (with > 0 && pairs(tab.len[with - 1]) <= t) --with;
+    cnt[t] = with;
+  }
+  tab.level_start[0] = 0;
+  for (int kl = 0; kl < tab.n_levels; ++kl)
+    tab.level_start[kl + 1] = tab.level_start[kl] + cnt[tab.n_levels - 1 - kl] * Hq;
+  zyfa::AttnArgs a{};
+  a.B = 1; a.S = T; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o; a.o_sb = o3[0]; a.o_ss = o3[1]; a.o_sh = o3[2];
+  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.debug_stall = g_debug_stall;
+  a.num_sms = d->sm_count;
+  a.scale_blocks = (max_len + 127) / 128;
+  cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
+                      : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");
+  return ZYFA_OK;
+}
+
+int zyfa_attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens, int B,
+                              int Hq, int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                              const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
+                              void* stream) {
+  return attn_varlen(false, q, nullptr, k, nullptr, v, nullptr, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream);
+}
+
+int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                             const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens, int B, int Hq,
+                             int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                             const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
+                             void* stream) {
+  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream);
+}
+
+int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                             const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream) {
+  int T = 0, max_len = 0;
+  if (int r = read_seqlens(cu_seqlens, B, &T, &max_len)) return r;
+  if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
+  if (H < 1 || H > 65535) return fail(ZYFA_ERR_INVALID_ARG, "H must be in 1..65535");
+  if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
+  if (hadamard && D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(scales, 4) || stride_t <= 0 || stride_h <= 0 ||
+      stride_t % 8 != 0 || stride_h % 8 != 0 || stride_t >= (int64_t(1) << 38) || stride_h >= (int64_t(1) << 38))
+    return fail(ZYFA_ERR_UNSUPPORTED,
+                "packed input needs 16-byte aligned x/out and token/head strides that are multiples of 8 elements");
+  if (T == 0) return ZYFA_OK;
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  zyfa::QuantArgs a{x, stride_t * T, stride_t, stride_h, static_cast<uint8_t*>(out), scales, 1, T, H, D, hadamard,
+                    d->status, g_timeout_ns, d->sm_count};
+  CUtensorMap tm;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 1};
+  const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(stride_h) * 2, static_cast<cuuint64_t>(stride_t) * 2,
+                                  static_cast<cuuint64_t>(stride_t) * 2 * static_cast<cuuint64_t>(T)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1u, 128u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult cr = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, gstrides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(x) failed: %d", (int)cr);
+  static thread_local zyfa::QuantSeqTable tab;
+  tab.n_seqs = B;
+  tab.max_blocks = (max_len + 127) / 128;
+  tab.cum_blocks[0] = 0;
+  for (int i = 0; i < B; ++i) {
+    tab.start[i] = cu_seqlens[i];
+    tab.len[i] = cu_seqlens[i + 1] - cu_seqlens[i];
+    tab.cum_blocks[i + 1] = tab.cum_blocks[i] + (tab.len[i] + 127) / 128;
+  }
+  cudaError_t e = zyfa::launch_quantize_fp8_stream_varlen(tm, a, tab, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
+  return ZYFA_OK;
 }
 
 int zyfa_get_device_status(void* stream, unsigned int* word) {

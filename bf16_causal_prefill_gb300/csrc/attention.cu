@@ -37,6 +37,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -114,9 +116,12 @@ struct Cfg {
 };
 
 struct Unit {
-  int b, hq, t;
+  int b, hq, t;            // batch coordinate of the maps (0 for packed input), query head, pair
   bool has_b;
   int n_a, n_b, n_kv;
+  int row0;                // first token of the sequence in the token dimension
+  int len;                 // tokens of the sequence
+  int sidx;                // sequence index of the scale arrays
 };
 
 // Work order. The (batch, KV head) groups are taken kGroupsInFlight at a
@@ -151,8 +156,54 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
   w.n_a = 2 * w.t + 1;
   w.n_b = 2 * w.t + 2;
   w.n_kv = w.has_b ? w.n_b : w.n_a;
+  w.row0 = 0;
+  w.sidx = w.b;
   return w;
 }
+
+// Unit lists. Equal lengths: B * Hq * pairs units decoded arithmetically
+// (decode_unit). Packed variable lengths: the host-built level table.
+struct NoTable {};
+
+template <bool VARLEN>
+struct Sched {
+  using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
+  const Table* tab;
+  int B, Hq, Hkv, S, n_qtiles;
+  __device__ __forceinline__ int n_units() const {
+    if constexpr (VARLEN) return tab->level_start[tab->n_levels];
+    else return B * Hq * ((n_qtiles + 1) / 2);
+  }
+  __device__ __forceinline__ Unit decode(int u) const {
+    if constexpr (VARLEN) {
+      // level k: the largest with level_start[k] <= u
+      int lo = 0, hi = tab->n_levels - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab->level_start[mid] <= u) lo = mid; else hi = mid - 1;
+      }
+      const int r = u - tab->level_start[lo];
+      const int rank = r / Hq;
+      Unit w;
+      w.b = 0;
+      w.hq = r - rank * Hq;
+      w.t = tab->n_levels - 1 - lo;
+      w.row0 = tab->start[rank];
+      w.len = tab->len[rank];
+      w.sidx = tab->index[rank];
+      const int nq = (w.len + 127) / 128;
+      w.has_b = (2 * w.t + 1) < nq;
+      w.n_a = 2 * w.t + 1;
+      w.n_b = 2 * w.t + 2;
+      w.n_kv = w.has_b ? w.n_b : w.n_a;
+      return w;
+    } else {
+      Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles);
+      w.len = S;
+      return w;
+    }
+  }
+};
 
 template <int DQK, bool FP8>
 struct Smem {
@@ -218,15 +269,15 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 // issues the TMA copies and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
-template <int DQK, bool FP8, int STREAM>
+template <int DQK, bool FP8, int STREAM, bool VARLEN>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
-                            const AttnArgs& a, int n_qtiles, bool leader) {
+                            const AttnArgs& a, const Sched<VARLEN>& sc, bool leader) {
   using C = Cfg<DQK, FP8>;
   constexpr bool kIsK = (STREAM == kStreamQK);
   constexpr int kStages = kIsK ? C::kNK : C::kNV;
   constexpr int kBlocks = kIsK ? C::kQkBlocks : C::kVBlocks;
   constexpr uint32_t kTileBytes = kIsK ? C::kQkTileBytes : C::kVTileBytes;
-  const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
+  const int n_units = sc.n_units();
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = sm.abort_flag();
   int st = 0;
@@ -240,7 +291,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   auto empty = [&](int i) { return kIsK ? sm.k_empty(i) : sm.v_empty(i); };
   auto tile = [&](int i) { return kIsK ? sm.k_tile(i) : sm.v_tile(i); };
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
+    const Unit w = sc.decode(u);
     const int hkv = w.hq / group;
     if constexpr (kIsK) {
       if (!(ok = warp_wait(sm.q_empty(), (qn & 1u) ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
@@ -249,12 +300,13 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
         mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
 #pragma unroll
         for (int kb = 0; kb < C::kQkBlocks; ++kb)
-          tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, 2 * w.t * 128, w.b);
+          tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq,
+                      w.row0 + 2 * w.t * 128, w.b);
         if (w.has_b) {
 #pragma unroll
           for (int kb = 0; kb < C::kQkBlocks; ++kb)
             tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq,
-                        (2 * w.t + 1) * 128, w.b);
+                        w.row0 + (2 * w.t + 1) * 128, w.b);
         }
       }
       ++qn;
@@ -267,7 +319,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
         mbar_arrive_expect_tx(full(st), kTileBytes);
 #pragma unroll
         for (int kb = 0; kb < kBlocks; ++kb)
-          tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, j * 128, w.b);
+          tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, w.row0 + j * 128, w.b);
       }
       par = (par & ~(1u << st)) | (ph << st);
       issued |= 1u << st;
@@ -334,10 +386,11 @@ __device__ __forceinline__ void issue_pv(const OperandDescs& od, uint32_t tmem_p
 // The whole warp runs the schedule (waits, stage and phase bookkeeping,
 // descriptors: all warp-uniform); one elected lane issues tcgen05.mma and
 // tcgen05.commit, so a commit tracks exactly the MMAs of that lane.
-template <int DQK, bool FP8>
-__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, int n_qtiles, bool leader) {
+template <int DQK, bool FP8, bool VARLEN>
+__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
+                         bool leader) {
   using C = Cfg<DQK, FP8>;
-  const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
+  const int n_units = sc.n_units();
   volatile int* abort_flag = sm.abort_flag();
   const uint32_t tS0 = tmem, tS1 = tmem + 128;
   const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
@@ -361,7 +414,7 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
   tc_fence_after();
 
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
+    const Unit w = sc.decode(u);
     do {
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
@@ -575,11 +628,11 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
 // with no measurable change in the output error.
 constexpr float kWinLo = -4.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
 
-template <int DQK, bool FP8>
-__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, int n_qtiles,
+template <int DQK, bool FP8, bool VARLEN>
+__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
                              int warp, int lane) {
-  const int n_units = a.B * a.Hq * ((n_qtiles + 1) / 2);
-  const int nblk = n_qtiles;
+  const int n_units = sc.n_units();
+  const int nblk = a.scale_blocks;
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = sm.abort_flag();
   const int wg = warp >> 2;                      // 0: tile 2t, 1: tile 2t+1
@@ -596,7 +649,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o);
 
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, a.B, a.Hq, a.Hkv, n_qtiles);
+    const Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
     const int qt = 2 * w.t + wg;
     const int n = qt + 1;
@@ -609,9 +662,9 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const float* ks_row = nullptr;
     const float* vs_row = nullptr;
     if constexpr (FP8) {
-      sq = __ldg(a.q_scale + (static_cast<int64_t>(w.b) * a.Hq + w.hq) * nblk + qt);
-      ks_row = a.k_scale + (static_cast<int64_t>(w.b) * a.Hkv + hkv) * nblk;
-      vs_row = a.v_scale + (static_cast<int64_t>(w.b) * a.Hkv + hkv) * nblk;
+      sq = __ldg(a.q_scale + (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt);
+      ks_row = a.k_scale + (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
+      vs_row = a.v_scale + (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
     }
     for (int j = 0; j < n; ++j) {
       float cj = a.scale_log2, lsv = 0.f, inv_sv = 1.f;
@@ -726,7 +779,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     tc_fence_after();
     const float inv = 1.f / l;
     const int q_row = qt * 128 + r;
-    __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(q_row) * a.o_ss + w.hq * a.o_sh;
+    __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(w.row0 + q_row) * a.o_ss + w.hq * a.o_sh;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
@@ -735,7 +788,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       uint32_t pko[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) pko[e] = pack_bf16x2(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
-      if (q_row < a.S) {
+      if (q_row < w.len) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
         for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pko[4 * v], pko[4 * v + 1], pko[4 * v + 2], pko[4 * v + 3]);
@@ -746,17 +799,24 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8>
+template <int DQK, bool FP8, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
+                    const __grid_constant__ typename Sched<VARLEN>::Table tab) {
   using C = Cfg<DQK, FP8>;
   extern __shared__ uint8_t smem_raw[];
   Smem<DQK, FP8> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_qtiles = (a.S + 127) / 128;
+  Sched<VARLEN> sc;
+  sc.tab = &tab;
+  sc.B = a.B;
+  sc.Hq = a.Hq;
+  sc.Hkv = a.Hkv;
+  sc.S = a.S;
+  sc.n_qtiles = (a.S + 127) / 128;
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
@@ -790,16 +850,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK>(sm, &tm_q, &tm_k, a, n_qtiles, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK>(sm, &tm_q, &tm_k, a, sc, leader);
     } else if (warp == kLoadWarpV) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV>(sm, &tm_q, &tm_v, a, n_qtiles, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV>(sm, &tm_q, &tm_v, a, sc, leader);
     } else if (warp == kMmaWarp) {
-      mma_role(sm, tmem, a, n_qtiles, leader);
+      mma_role(sm, tmem, a, sc, leader);
     }
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role(sm, tmem, a, n_qtiles, warp, lane);
+    softmax_role(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -810,33 +870,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8>
+template <int DQK, bool FP8, bool VARLEN>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
-                   cudaStream_t stream) {
+                   const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int n_qtiles = (a.S + 127) / 128;
-  const long long n_units = static_cast<long long>(a.B) * a.Hq * ((n_qtiles + 1) / 2);
+  if (n_units == 0) return cudaSuccess;
   const int grid = static_cast<int>(n_units < a.num_sms ? n_units : a.num_sms);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab);
   return cudaGetLastError();
+}
+
+long long fixed_units(const AttnArgs& a) {
+  const int n_qtiles = (a.S + 127) / 128;
+  return static_cast<long long>(a.B) * a.Hq * ((n_qtiles + 1) / 2);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const AttnArgs& a, cudaStream_t stream) {
-  if (a.Dqk == 128) return launch<128, false>(tm_q, tm_k, tm_v, a, stream);
-  if (a.Dqk == 192) return launch<192, false>(tm_q, tm_k, tm_v, a, stream);
+  const NoTable none{};
+  if (a.Dqk == 128) return launch<128, false, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
+  if (a.Dqk == 192) return launch<192, false, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const AttnArgs& a, cudaStream_t stream) {
-  if (a.Dqk == 128) return launch<128, true>(tm_q, tm_k, tm_v, a, stream);
-  if (a.Dqk == 192) return launch<192, true>(tm_q, tm_k, tm_v, a, stream);
+  const NoTable none{};
+  if (a.Dqk == 128) return launch<128, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
+  if (a.Dqk == 192) return launch<192, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
+  const long long n = tab.level_start[tab.n_levels];
+  if (a.Dqk == 128) return launch<128, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.Dqk == 192) return launch<192, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
+  const long long n = tab.level_start[tab.n_levels];
+  if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -10,6 +10,8 @@ namespace zyfa {
 
 constexpr int kBlockTokens = 128;   // quantisation block and attention tile height
 constexpr int kTileKeys = 128;      // keys per K/V tile
+constexpr int kMaxVarlenSeqs = 1024;     // sequences of a packed batch
+constexpr int kMaxVarlenLevels = 1024;   // pairs of 128-row query tiles: 256K tokens
 
 struct QuantArgs {
   const void* x;          // bf16 [B,S,H,D], element strides sb, ss, sh; last dim contiguous
@@ -23,15 +25,44 @@ struct QuantArgs {
   int num_sms;
 };
 
+// Packed variable-length input to the quantiser: sequence i is tokens
+// start[i] .. start[i] + len[i] - 1; its 128-token blocks are numbered from
+// cum_blocks[i]; scales are [n_seqs, H, max_blocks].
+struct QuantSeqTable {
+  int n_seqs;
+  int max_blocks;
+  int start[kMaxVarlenSeqs];
+  int len[kMaxVarlenSeqs];
+  int cum_blocks[kMaxVarlenSeqs + 1];
+};
+
 // Register kernel: any 4-byte aligned input with even strides.
 cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
 // Streaming kernel: persistent CTAs, TMA ring of input blocks. tm_x is a 4-D
 // map (D, H, S, B) over x, no swizzle, box D x 1 x 128 x 1 (needs a 16-byte
 // aligned base and strides that are multiples of 8 elements).
 cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream);
+// Streaming kernel over a packed variable-length tensor (B = 1, S = total
+// tokens in `a`; tm_x over (D, H, T, 1)).
+cudaError_t launch_quantize_fp8_stream_varlen(const CUtensorMap& tm_x, const QuantArgs& a, const QuantSeqTable& tab,
+                                              cudaStream_t stream);
+
+// Variable-length batches: sequences packed along the token dimension. The
+// host sorts the sequences by length (longest first) and lays out the unit
+// list by "levels": level k holds pair index t = n_levels - 1 - k of every
+// sequence that has more than t pairs of 128-row query tiles (a prefix of the
+// sorted order), query heads adjacent. Passed to the kernels by value.
+struct SeqTable {
+  int n_seqs;                          // sequences with at least one token
+  int n_levels;                        // pairs of query tiles of the longest
+  int start[kMaxVarlenSeqs];           // first token, sorted order
+  int len[kMaxVarlenSeqs];             // tokens, sorted order (descending)
+  int index[kMaxVarlenSeqs];           // position in the caller's batch
+  int level_start[kMaxVarlenLevels + 1];   // first unit of each level
+};
 
 struct AttnArgs {
-  int B, S, Hq, Hkv, Dqk, Dv;
+  int B, S, Hq, Hkv, Dqk, Dv;         // varlen: B = 1 and S = total tokens (the packed tensor)
   float scale_log2;        // softmax_scale * log2(e)
   void* o;                 // bf16 [B,S,Hq,Dv]
   int64_t o_sb, o_ss, o_sh;
@@ -42,6 +73,7 @@ struct AttnArgs {
   uint64_t timeout_ns;     // bound on every barrier wait
   int debug_stall;         // nonzero: the loader issues nothing (watchdog test)
   int num_sms;
+  int scale_blocks;        // fp8: blocks per (sequence, head) row of the scale arrays
 };
 
 // tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of
@@ -50,5 +82,10 @@ cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
                              const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const AttnArgs& a, cudaStream_t stream);
+// Packed variable-length batch: maps over (D, H, T, 1); `tab` as above.
+cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream);
+cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const AttnArgs& a, const SeqTable& tab, cudaStream_t stream);
 
 }  // namespace zyfa

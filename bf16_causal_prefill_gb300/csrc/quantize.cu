@@ -21,6 +21,8 @@
 // shuffles while spans 1 and 64 stay in registers.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -156,9 +158,20 @@ struct StreamCfg {
   static constexpr int kSmemBytes = kStages * kBlockBytes + 1024;
 };
 
-template <int D, bool kHadamard>
+struct NoQuantTable {};
+
+// One 128-token block of the walk: map coordinates (b, h, tok), the number of
+// its rows inside the sequence, and where its scale goes.
+struct QBlock {
+  int b, h, tok, valid;
+  int64_t scale_idx;
+};
+
+template <int D, bool kHadamard, bool VARLEN>
 __global__ void __launch_bounds__(kStreamThreads, 1)
-    quantize_fp8_stream_kernel(const __grid_constant__ CUtensorMap tm_x, QuantArgs a) {
+    quantize_fp8_stream_kernel(const __grid_constant__ CUtensorMap tm_x, QuantArgs a,
+                               const __grid_constant__ typename std::conditional<VARLEN, QuantSeqTable,
+                                                                                 NoQuantTable>::type tab) {
   using SC = StreamCfg<D>;
   constexpr int kGroups = D / 64;   // 8-element groups per lane and row
   static_assert(!kHadamard || D == 128, "rotation is defined for head dim 128");
@@ -169,20 +182,44 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
-  const long long total = static_cast<long long>(a.B) * a.H * nblk;
+  long long total;
+  if constexpr (VARLEN) total = static_cast<long long>(a.H) * tab.cum_blocks[tab.n_seqs];
+  else total = static_cast<long long>(a.B) * a.H * nblk;
   const long long first = blockIdx.x, step = gridDim.x;
 
-  auto coords = [&](long long g, int& b, int& h, int& blk) {
-    blk = static_cast<int>(g % nblk);
-    const long long bh = g / nblk;
-    h = static_cast<int>(bh % a.H);
-    b = static_cast<int>(bh / a.H);
+  // Equal lengths: blocks in (b, h, blk) order. Packed sequences: sequence
+  // by sequence (binary search on the block prefix), then (h, blk).
+  auto coords = [&](long long g) {
+    QBlock q;
+    if constexpr (VARLEN) {
+      int lo = 0, hi = tab.n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<long long>(a.H) * tab.cum_blocks[mid] <= g) lo = mid; else hi = mid - 1;
+      }
+      const int nb = tab.cum_blocks[lo + 1] - tab.cum_blocks[lo];
+      const int r = static_cast<int>(g - static_cast<long long>(a.H) * tab.cum_blocks[lo]);
+      q.h = r / nb;
+      const int blk = r - q.h * nb;
+      q.b = 0;
+      q.tok = tab.start[lo] + blk * kBlockTokens;
+      q.valid = min(kBlockTokens, tab.len[lo] - blk * kBlockTokens);
+      q.scale_idx = (static_cast<int64_t>(lo) * a.H + q.h) * tab.max_blocks + blk;
+    } else {
+      const int blk = static_cast<int>(g % nblk);
+      const long long bh = g / nblk;
+      q.h = static_cast<int>(bh % a.H);
+      q.b = static_cast<int>(bh / a.H);
+      q.tok = blk * kBlockTokens;
+      q.valid = min(kBlockTokens, a.S - blk * kBlockTokens);
+      q.scale_idx = (static_cast<int64_t>(q.b) * a.H + q.h) * nblk + blk;
+    }
+    return q;
   };
   auto issue = [&](long long g, int st) {
-    int b, h, blk;
-    coords(g, b, h, blk);
+    const QBlock q = coords(g);
     mbar_arrive_expect_tx(&full[st], SC::kBlockBytes);
-    tma_load_4d(buf + st * SC::kBlockBytes, &tm_x, &full[st], 0, h, blk * kBlockTokens, b);
+    tma_load_4d(buf + st * SC::kBlockBytes, &tm_x, &full[st], 0, q.h, q.tok, q.b);
   };
 
   if (threadIdx.x == 0) {
@@ -201,8 +238,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   for (long long g = first; g < total; g += step, ++it) {
     const int st = it % SC::kStages;
     const uint32_t par = static_cast<uint32_t>(it / SC::kStages) & 1u;
-    int b, h, blk;
-    coords(g, b, h, blk);
+    const QBlock qb = coords(g);
     const bool ok = mbar_wait(&full[st], par, &abort_flag, a.status, kStatusQuantTimeout, a.timeout_ns);
 
     // v[g][k*8 + e]: row warp*8 + 4*g + lane/8, element 64*k + 8*(lane%8) + e
@@ -222,6 +258,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
             v[g2][8 * k + 2 * e] = f.x;
             v[g2][8 * k + 2 * e + 1] = f.y;
+          }
+        }
+        if constexpr (VARLEN) {
+          // rows past the sequence's end belong to the next sequence
+          if (r >= qb.valid) {
+#pragma unroll
+            for (int e = 0; e < kGroups * 8; ++e) v[g2][e] = 0.f;
           }
         }
         if constexpr (kHadamard) {
@@ -271,12 +314,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     for (int w = 1; w < kStreamThreads / 32; ++w) bmax = fmaxf(bmax, red[it & 1][w]);
     const float scale = (bmax < kZeroGuard) ? 1.0f : __fdiv_rn(bmax, kE4m3Max);
     const float rinv = __frcp_rn(scale);
-    if (threadIdx.x == 0) a.scales[(static_cast<int64_t>(b) * a.H + h) * nblk + blk] = scale;
+    if (threadIdx.x == 0) a.scales[qb.scale_idx] = scale;
 #pragma unroll
     for (int g2 = 0; g2 < 2; ++g2) {
-      const int s = blk * kBlockTokens + warp * kStreamRowsPerWarp + 4 * g2 + (lane >> 3);
-      if (s < a.S) {
-        uint8_t* orow = a.out + ((static_cast<int64_t>(b) * a.S + s) * a.H + h) * D + 8 * (lane & 7);
+      const int rr = warp * kStreamRowsPerWarp + 4 * g2 + (lane >> 3);
+      if (rr < qb.valid) {
+        const int64_t s = static_cast<int64_t>(qb.b) * a.S + qb.tok + rr;
+        uint8_t* orow = a.out + (s * a.H + qb.h) * D + 8 * (lane & 7);
 #pragma unroll
         for (int k = 0; k < kGroups; ++k) {
           uint32_t w[4];
@@ -318,21 +362,33 @@ cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, bool H>
-static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream) {
-  auto kern = quantize_fp8_stream_kernel<D, H>;
+template <int D, bool H, bool VARLEN, typename Table>
+static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, const Table& tab, long long total,
+                                 cudaStream_t stream) {
+  auto kern = quantize_fp8_stream_kernel<D, H, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long total = static_cast<long long>(a.B) * a.H * ((a.S + kBlockTokens - 1) / kBlockTokens);
+  if (total == 0) return cudaSuccess;
   const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
-  kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a);
+  kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a, tab);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream) {
-  if (a.D == 128 && a.hadamard) return launch_stream<128, true>(tm_x, a, stream);
-  if (a.D == 128) return launch_stream<128, false>(tm_x, a, stream);
-  if (a.D == 192) return launch_stream<192, false>(tm_x, a, stream);
+  const NoQuantTable none{};
+  const long long total = static_cast<long long>(a.B) * a.H * ((a.S + kBlockTokens - 1) / kBlockTokens);
+  if (a.D == 128 && a.hadamard) return launch_stream<128, true, false>(tm_x, a, none, total, stream);
+  if (a.D == 128) return launch_stream<128, false, false>(tm_x, a, none, total, stream);
+  if (a.D == 192) return launch_stream<192, false, false>(tm_x, a, none, total, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_fp8_stream_varlen(const CUtensorMap& tm_x, const QuantArgs& a, const QuantSeqTable& tab,
+                                              cudaStream_t stream) {
+  const long long total = static_cast<long long>(a.H) * tab.cum_blocks[tab.n_seqs];
+  if (a.D == 128 && a.hadamard) return launch_stream<128, true, true>(tm_x, a, tab, total, stream);
+  if (a.D == 128) return launch_stream<128, false, true>(tm_x, a, tab, total, stream);
+  if (a.D == 192) return launch_stream<192, false, true>(tm_x, a, tab, total, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -109,12 +109,14 @@ int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int
  * Causal attention on per-block FP8 inputs ("ZYFA ...", "Per-Block Scaling
  * and Normalization by the Rounded Row Sum"). Inputs are e4m3 codes with one
  * fp32 scale per (b, h, 128-token block), as written by zyfa_quantize_fp8;
- * the dequantised value is code * scale. Within each 128-key tile the
- * probabilities of a row are multiplied by a power of two that puts their
- * maximum in (0.5, 1], rounded to e4m3 (RNE), multiplied by V on the tensor
- * cores with fp32 accumulation, and each row is divided by the sum of the
- * rounded probabilities (the power of two divided back out), so the weights
- * that multiply V sum to one. Output bf16.
+ * the dequantised value is code * scale. Each row keeps an offset: its
+ * probabilities, times the key tile's V scale and divided by 2^offset, are
+ * rounded to e4m3 (RNE); the offset is set from the first key tile's maximum
+ * and moved (rescaling the output so far) when a tile's largest rounded value
+ * would leave [2^-4, 2^8]. The rounded values multiply the V codes on the
+ * tensor cores with fp32 accumulation, and each row is divided by the sum of
+ * the same rounded values (offset and V scale divided back out), so the
+ * weights that multiply V sum to one. Output bf16.
  *
  * q8/k8/v8 : uint8 e4m3 [B,S,H,D] with the given strides (multiples of 16
  *            elements), 16-byte aligned.
@@ -127,10 +129,52 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
                       const int64_t v_strides[3], const int64_t o_strides[3], void* stream);
 
 /*
+ * Packed variable-length batches. The pages time equal-length batches and
+ * name variable lengths as future work ("ZYFA ...", "Methodology and
+ * Limitations"); this is the layout serving stacks use. Sequences are packed
+ * along the token dimension: sequence i is tokens cu_seqlens[i] ..
+ * cu_seqlens[i+1]-1 of q [T,Hq,Dqk], k [T,Hkv,Dqk], v [T,Hkv,Dv] and
+ * o [T,Hq,Dv] (T = cu_seqlens[B]) and attends causally within itself only.
+ *
+ * cu_seqlens : HOST int32 [B+1]: cu_seqlens[0] = 0, nondecreasing;
+ *              1 <= B <= 1024, each sequence at most 262144 tokens, empty
+ *              sequences allowed (T = 0 enqueues nothing).
+ * *_strides  : [2] element strides of the token and head dimensions (the
+ *              last dimension contiguous); alignment rules as above.
+ * q/k/v_scale (FP8): float [B, H, ceil(max_len/128)], one per (sequence,
+ *              head, 128-token block of that sequence), as written by
+ *              zyfa_quantize_fp8_varlen.
+ * The host builds the work list from cu_seqlens (longest sequences first)
+ * and passes it to the kernel by value; nothing is allocated.
+ * Errors as the equal-length calls.
+ */
+int zyfa_attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens, int B,
+                              int Hq, int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                              const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
+                              void* stream);
+int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                             const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens, int B, int Hq,
+                             int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                             const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
+                             void* stream);
+
+/*
+ * zyfa_quantize_fp8 for a packed variable-length tensor x [T,H,D] (same
+ * arithmetic, bit for bit). Blocks are 128 tokens of one sequence; the last
+ * block of a sequence may be short and tokens of the next sequence never
+ * enter its amax. out: uint8 e4m3 [T,H,D] dense; scales: float
+ * [B, H, ceil(max_len/128)] (entries past a sequence's last block are not
+ * written). Needs 16-byte aligned x and out and token/head strides that are
+ * multiples of 8 elements (ZYFA_ERR_UNSUPPORTED otherwise).
+ */
+int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                             const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. *word receives the raw bits (0 when every kernel finished normally;
  * bit 0: loader wait timed out, bit 1: MMA wait, bit 2: softmax wait,
- * bit 8: drain after abort incomplete). Returns ZYFA_ERR_TIMEOUT if any bit
+ * bit 3: quantiser wait, bit 8: drain after abort incomplete). Returns ZYFA_ERR_TIMEOUT if any bit
  * was set, ZYFA_ERR_CUDA if the synchronisation failed, else ZYFA_OK.
  * `word` may be NULL.
  */

@@ -58,6 +58,23 @@ def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) 
     return out
 
 
+def causal_attention_varlen(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens, scale: float) -> np.ndarray:
+    """Packed variable-length batch: q [T,Hq,Dqk], k [T,Hkv,Dqk], v [T,Hkv,Dv];
+    sequence i is tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and attends
+    causally within itself only (the same definition applied to each
+    sequence). Returns O [T,Hq,Dv] float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros((q.shape[0], q.shape[1], v.shape[2]), dtype=np.float64)
+    cu = [int(x) for x in cu_seqlens]
+    for i in range(len(cu) - 1):
+        s, e = cu[i], cu[i + 1]
+        if e > s:
+            out[s:e] = causal_attention(q[None, s:e], k[None, s:e], v[None, s:e], scale)[0]
+    return out
+
+
 def causal_attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                           b: int, h: int, rows: Iterable[int]) -> np.ndarray:
     """Selected output rows of one (batch, query head), one row at a time:

@@ -134,6 +134,39 @@ def quantize_fp8(x: np.ndarray, hadamard: bool = False, block: int = BLOCK_TOKEN
     return np.ascontiguousarray(codes), np.ascontiguousarray(scale.transpose(0, 2, 1))
 
 
+def quantize_fp8_varlen(x: np.ndarray, cu_seqlens, hadamard: bool = False, block: int = BLOCK_TOKENS):
+    """Packed variable-length x [T,H,D]: each sequence quantised on its own
+    (its 128-token blocks never mix tokens of two sequences). Returns codes
+    uint8 [T,H,D] and scales float32 [B,H,ceil(max_len/128)]; entries past a
+    sequence's last block are NaN (never written)."""
+    x = np.asarray(x)
+    cu = [int(c) for c in cu_seqlens]
+    B = len(cu) - 1
+    max_len = max(cu[i + 1] - cu[i] for i in range(B))
+    nb = (max_len + block - 1) // block
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    scales = np.full((B, x.shape[1], nb), np.nan, dtype=np.float32)
+    for i in range(B):
+        s, e = cu[i], cu[i + 1]
+        if e > s:
+            c, sc = quantize_fp8(x[None, s:e], hadamard=hadamard, block=block)
+            codes[s:e] = c[0]
+            scales[i, :, :sc.shape[2]] = sc[0]
+    return codes, scales
+
+
+def dequantize_fp8_varlen(codes: np.ndarray, scales: np.ndarray, cu_seqlens, block: int = BLOCK_TOKENS):
+    """Inverse of quantize_fp8_varlen: float64 [T,H,D]."""
+    cu = [int(c) for c in cu_seqlens]
+    out = np.zeros(codes.shape, dtype=np.float64)
+    for i in range(len(cu) - 1):
+        s, e = cu[i], cu[i + 1]
+        if e > s:
+            nb = (e - s + block - 1) // block
+            out[s:e] = dequantize_fp8(codes[None, s:e], scales[i:i + 1, :, :nb], block=block)[0]
+    return out
+
+
 def dequantize_fp8(codes: np.ndarray, scales: np.ndarray, block: int = BLOCK_TOKENS):
     """codes [B,S,H,D] uint8, scales [B,H,nblk] -> float64 [B,S,H,D] = code * scale."""
     vals = e4m3_decode(codes)

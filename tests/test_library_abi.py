@@ -90,3 +90,47 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 128, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         zyfa.quantize_fp8(x)
+
+
+I2 = ctypes.c_int64 * 2
+
+
+def _cu(*vals):
+    return (ctypes.c_int32 * len(vals))(*vals)
+
+
+def _varlen(L, cu, B, **kw):
+    a = dict(q=16, k=16, v=16, o=16, Hq=2, Hkv=1, Dqk=128, Dv=128, scale=0.1,
+             qs=I2(256, 128), ks=I2(128, 128), vs=I2(128, 128), os_=I2(256, 128))
+    a.update(kw)
+    return L.zyfa_attn_fwd_bf16_varlen(a["q"], a["k"], a["v"], a["o"], cu, B, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"],
+                                       ctypes.c_float(a["scale"]), a["qs"], a["ks"], a["vs"], a["os_"], None)
+
+
+@pytest.mark.parametrize("cu,B,kw,code", [
+    (None, 1, {}, 1),                                # null cu_seqlens
+    (_cu(1, 5), 1, {}, 1),                           # cu_seqlens[0] != 0
+    (_cu(0, 5, 3), 2, {}, 1),                        # decreasing
+    (_cu(0, 5), 0, {}, 1),                           # no sequence
+    (_cu(0, 300000), 1, {}, 2),                      # longer than the level table
+    (_cu(0, 5, 9), 2, dict(Hq=3, Hkv=2), 1),         # Hq not a multiple of Hkv
+    (_cu(0, 5, 9), 2, dict(qs=I2(100, 128)), 1),     # token stride not 16-byte multiple
+    (_cu(0, 5, 9), 2, dict(Dqk=64, Dv=64), 2),
+])
+def test_varlen_attention_rejects_bad_arguments_on_host(L, cu, B, kw, code):
+    assert _varlen(L, cu, B, **kw) == code
+    assert L.zyfa_last_error_message()
+
+
+def test_varlen_empty_batch_enqueues_nothing(L):
+    # every sequence empty: valid, nothing to compute, no device touched
+    assert _varlen(L, _cu(0, 0, 0), 2) == 0
+
+
+def test_varlen_quantiser_rejects_bad_arguments_on_host(L):
+    q = L.zyfa_quantize_fp8_varlen
+    assert q(16, 128, 128, 16, 16, _cu(0, 4, 2), 2, 1, 128, 0, None) == 1    # decreasing offsets
+    assert q(16, 128, 128, 16, 16, _cu(0, 4), 1, 1, 64, 0, None) == 2         # D
+    assert q(16, 132, 128, 16, 16, _cu(0, 4), 1, 1, 128, 0, None) == 2        # token stride not a multiple of 8
+    assert q(8, 128, 128, 16, 16, _cu(0, 4), 1, 1, 128, 0, None) == 2         # base not 16-byte aligned
+    assert q(16, 128, 128, 16, 16, _cu(0, 0), 1, 1, 128, 0, None) == 0        # empty: nothing enqueued
