@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
                                            c_float, vp, vp, vp, vp, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    L.zyfa_set_fp8_probabilities.restype = c_int
+    L.zyfa_set_fp8_probabilities.argtypes = [c_int]
     L.zyfa_set_debug.restype = c_int
     L.zyfa_set_debug.argtypes = [c_int, ctypes.c_double]
     _lib = L
@@ -304,6 +306,15 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _check(lib().zyfa_get_device_status(s, ctypes.byref(w)))
     return w.value
+
+
+def set_fp8_probabilities(mode: str = "exact") -> None:
+    """FP8 attention probabilities: "exact" (default) or "lean" (head dim 128;
+    the e4m3 code approximated linearly, no exponential). Process-wide."""
+    modes = {"exact": 0, "lean": 1}
+    if mode not in modes:
+        raise ValueError(f"mode must be one of {sorted(modes)}")
+    _check(lib().zyfa_set_fp8_probabilities(modes[mode]))
 
 
 def set_debug(stall_loader: bool = False, timeout_seconds: float = 0.0) -> None:

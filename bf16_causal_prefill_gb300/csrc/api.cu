@@ -42,6 +42,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
 uint64_t g_timeout_ns = 2000000000ull;
+int g_lean_p = 0;   // FP8 probabilities: 0 exact, 1 lean (head dim 128)
 int g_debug_stall = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -174,6 +175,12 @@ int zyfa_set_debug(int stall_loader, double timeout_seconds) {
   return ZYFA_OK;
 }
 
+int zyfa_set_fp8_probabilities(int mode) {
+  if (mode != 0 && mode != 1) return fail(ZYFA_ERR_INVALID_ARG, "mode must be 0 (exact) or 1 (lean)");
+  g_lean_p = mode;
+  return ZYFA_OK;
+}
+
 int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
                       float* scales, int B, int S, int H, int D, int hadamard, void* stream) {
   if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
@@ -246,6 +253,7 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = (S + 127) / 128;
+  a.lean_p = g_lean_p;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
@@ -349,6 +357,7 @@ static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k,
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = (max_len + 127) / 128;
+  a.lean_p = g_lean_p;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");

@@ -546,38 +546,44 @@ __device__ __forceinline__ uint32_t pack_e4m3x4_sum(float v0, float v1, float v2
   return d;
 }
 
-#ifdef ZYFA_EX2_F16
-// Same, from f32 exponents: x rounded to f16 pairs, 2^x by the packed f16
-// exponential, then f16 pairs -> e4m3.
-__device__ __forceinline__ uint32_t exp2_e4m3x4_sum(float2 x01, float2 x23, float2& acc) {
+
+// Lean P ("ZYFA ...", "Lean P: Linear Approximation of the FP8 Code"): the
+// code of a positive e4m3 number grows by 8 per doubling, so the code of 2^x
+// is close to 8x + 56 (56 encodes 1.0). y = 1024 + 8x + 56 arrives from the
+// caller's multiply-add; converting it to f16 rounds to the nearest integer
+// (f16 spacing is 1 in [1024, 2048)) and leaves that integer in the low byte
+// of each half; a packed max with 1024 clamps negative codes to 0 (value 0).
+// The offset window keeps 8x <= 64, so codes stay <= 120. The four codes are
+// gathered with one byte permute; acc adds their exact values as in
+// pack_e4m3x4_sum.
+__device__ __forceinline__ uint32_t lean_e4m3x4_sum(float2 y01, float2 y23, float2& acc) {
   uint32_t d;
-  asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 x01, x23, e01, e23, h01, h23;\n\t"
-      "cvt.rn.f16x2.f32 x01, %4, %3;\n\t"
-      "cvt.rn.f16x2.f32 x23, %6, %5;\n\t"
-      "ex2.approx.f16x2 e01, x01;\n\t"
-      "ex2.approx.f16x2 e23, x23;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f16x2 lo, e01;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f16x2 hi, e23;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t"
-      "cvt.rn.f16x2.e4m3x2 h01, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 h23, hi;\n\t"
-      "mov.b32 {a0, a1}, h01;\n\t"
-      "mov.b32 {a2, a3}, h23;\n\t"
+  asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 h01, h23, e01, e23, k;\n\t"
+      "mov.b32 k, 0x64006400;\n\t"
+      "cvt.rn.f16x2.f32 h01, %4, %3;\n\t"
+      "cvt.rn.f16x2.f32 h23, %6, %5;\n\t"
+      "max.f16x2 h01, h01, k;\n\t"
+      "max.f16x2 h23, h23, k;\n\t"
+      "prmt.b32 %0, h01, h23, 0x6420;\n\t"
+      "mov.b32 {lo, hi}, %0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 e01, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 e23, hi;\n\t"
+      "mov.b32 {a0, a1}, e01;\n\t"
+      "mov.b32 {a2, a3}, e23;\n\t"
       "add.rn.f32.f16 %1, a0, %1;\n\t"
       "add.rn.f32.f16 %2, a1, %2;\n\t"
       "add.rn.f32.f16 %1, a2, %1;\n\t"
       "add.rn.f32.f16 %2, a3, %2;\n\t}"
       : "=r"(d), "+f"(acc.x), "+f"(acc.y)
-      : "f"(x01.x), "f"(x01.y), "f"(x23.x), "f"(x23.y));
+      : "f"(y01.x), "f"(y01.y), "f"(y23.x), "f"(y23.y));
   return d;
 }
-#endif
 
 // Probabilities of one 32-column chunk c, p = 2^(s * ca + cb):
 //   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the fp32 p.
 //   FP8:  e4m3 codes, four per word, into pk[8c .. 8c+7]; acc sums the
 //         rounded values.
-template <bool FP8>
+template <bool FP8, bool LEAN = false>
 __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, float cb, uint32_t* pk,
                                             float2 (&acc)[2]) {
   const float2 a2 = make_float2(ca, ca);
@@ -592,17 +598,22 @@ __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, 
       acc[i & 1] = __fadd2_rn(acc[i & 1], p);
     }
   } else {
+    // lean P: y = 1024 + 56 + 8x = s * (8 ca) + (8 cb + 1080)
+    const float2 la2 = make_float2(8.f * ca, 8.f * ca);
+    const float2 lb2 = make_float2(8.f * cb + 1080.f, 8.f * cb + 1080.f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float s0 = u2f(s[4 * i]), s1 = u2f(s[4 * i + 1]), s2 = u2f(s[4 * i + 2]), s3 = u2f(s[4 * i + 3]);
-      const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
-      const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
-#ifdef ZYFA_EX2_F16
-      pk[8 * c + i] = exp2_e4m3x4_sum(x01, x23, acc[i & 1]);
-#else
-      pk[8 * c + i] = pack_e4m3x4_sum(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y),
-                                      acc[i & 1]);
-#endif
+      if constexpr (LEAN) {
+        const float2 y01 = __ffma2_rn(make_float2(s0, s1), la2, lb2);
+        const float2 y23 = __ffma2_rn(make_float2(s2, s3), la2, lb2);
+        pk[8 * c + i] = lean_e4m3x4_sum(y01, y23, acc[i & 1]);
+      } else {
+        const float2 x01 = __ffma2_rn(make_float2(s0, s1), a2, b2);
+        const float2 x23 = __ffma2_rn(make_float2(s2, s3), a2, b2);
+        pk[8 * c + i] = pack_e4m3x4_sum(ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x),
+                                        ex2_approx(x23.y), acc[i & 1]);
+      }
     }
   }
 }
@@ -628,7 +639,7 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
 // with no measurable change in the output error.
 constexpr float kWinLo = -4.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
 
-template <int DQK, bool FP8, bool VARLEN>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN>
 __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
                              int warp, int lane) {
   const int n_units = sc.n_units();
@@ -719,7 +730,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         }
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) probs_chunk<true>(c, &s[32 * c], cj, lsv - m, pk, acc);
+        for (int c = 0; c < 4; ++c) probs_chunk<true, LEAN>(c, &s[32 * c], cj, lsv - m, pk, acc);
         const float2 t = __fadd2_rn(acc[0], acc[1]);
         psum = t.x + t.y;
         // O is final for the previous tiles (their PV completed before this
@@ -799,7 +810,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8, bool VARLEN>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
@@ -859,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role(sm, tmem, a, sc, warp, lane);
+    softmax_role<DQK, FP8, VARLEN, LEAN>(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -870,11 +881,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8, bool VARLEN>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN = false>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                    const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (n_units == 0) return cudaSuccess;
@@ -901,6 +912,7 @@ cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const AttnArgs& a, cudaStream_t stream) {
   const NoTable none{};
+  if (a.Dqk == 128 && a.lean_p) return launch<128, true, false, true>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
   if (a.Dqk == 128) return launch<128, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
   if (a.Dqk == 192) return launch<192, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
   return cudaErrorInvalidValue;
@@ -917,6 +929,7 @@ cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& 
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
   const long long n = tab.level_start[tab.n_levels];
+  if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;

@@ -74,6 +74,7 @@ struct AttnArgs {
   int debug_stall;         // nonzero: the loader issues nothing (watchdog test)
   int num_sms;
   int scale_blocks;        // fp8: blocks per (sequence, head) row of the scale arrays
+  int lean_p;              // fp8, head dim 128: lean P instead of exact P
 };
 
 // tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of

@@ -181,6 +181,19 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
 int zyfa_get_device_status(void* stream, unsigned int* word);
 
 /*
+ * How the FP8 attention calls compute the rounded probabilities (process-wide,
+ * not thread-safe; applies to calls enqueued afterwards):
+ *   0: exact P (default): 2^x by the exponential unit, then RNE to e4m3;
+ *   1: lean P ("ZYFA ...", "Lean P: Linear Approximation of the FP8 Code"):
+ *      the e4m3 code of 2^x approximated by round(8x + 56), no exponential;
+ *      head dim 128 only (the MLA shape keeps exact P, as on the pages).
+ *      Faster, with a larger probability-rounding error (the normalisation
+ *      by the rounded row sum still holds exactly).
+ * Returns ZYFA_ERR_INVALID_ARG for another mode.
+ */
+int zyfa_set_fp8_probabilities(int mode);
+
+/*
  * Test hooks (process-wide, not thread-safe). stall_loader != 0 makes the
  * attention kernels' loader warp issue nothing, so every consumer wait runs
  * out; timeout_seconds bounds each wait (default 2.0; <= 0 restores it).

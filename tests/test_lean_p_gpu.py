@@ -1,0 +1,82 @@
+"""Lean P ("ZYFA ...", "Lean P: Linear Approximation of the FP8 Code"), an
+opt-in mode of the FP8 attention at head dim 128: the e4m3 code of 2^x is
+approximated by round(8x + 56) instead of an exponential followed by RNE.
+
+- the normalisation by the rounded row sum still makes constant V come back
+  exactly (the pin of the exact path);
+- its error against the oracle on the dequantised inputs is reported as a
+  multiple of exact P's on the same rows; on the activation-like workload
+  (the stand-in for the pages' captured layers) it stays within the 1.4x the
+  pages' 1.22-1.36x suggests, and every workload stays within the FP8 gate
+  at full size;
+- the MLA shape keeps exact P (bitwise equal in both modes).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bf16_causal_prefill_gb300 as zyfa
+import workloads
+from parity import (FP8_REL_L2, f32, fp8_quant_blocks_for_rows, gpu_rows, oracle_dequant, oracle_quant,
+                    sampled_rows_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    zyfa.set_fp8_probabilities("exact")
+
+
+def _run(mode, q, k, v, had):
+    zyfa.set_fp8_probabilities(mode)
+    try:
+        o, _ = zyfa.prefill_fp8(q, k, v, hadamard=had)
+        zyfa.device_status()
+    finally:
+        zyfa.set_fp8_probabilities("exact")
+    return o
+
+
+def test_lean_p_keeps_the_exact_average():
+    g = torch.Generator().manual_seed(11)
+    B, S, Hq, Hkv, D = 1, 700, 4, 2, 128
+    q = (torch.randn(B, S, Hq, D, generator=g) * 4).to(torch.bfloat16).cuda()
+    k = (torch.randn(B, S, Hkv, D, generator=g) * 4).to(torch.bfloat16).cuda()
+    c = 448.0 * 2 ** -5
+    v = torch.full((B, S, Hkv, 128), c).to(torch.bfloat16).cuda()
+    o = _run("lean", q, k, v, False)
+    assert torch.equal(o.float().cpu(), torch.full((B, S, Hq, 128), c))
+
+
+def test_mla_shape_keeps_exact_p():
+    w = workloads.custom(1, 2, 2, 640, Dqk=192, Dv=128, seed=5)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    assert torch.equal(_run("lean", q, k, v, False), _run("exact", q, k, v, False))
+
+
+@pytest.mark.parametrize("name,had,max_ratio", [("act_b1_gqa32x8_s16k_d128", False, 1.4),
+                                                ("act_b1_gqa32x8_s16k_d128", True, 1.4),
+                                                ("gauss_b1_gqa32x8_s32k_d128", False, None)])
+def test_lean_p_error_against_exact_p(name, had, max_ratio):
+    w = workloads.get(name)
+    q, k, v = workloads.make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rows = workloads.sample_rows(w.S, n=6, seed=w.S + 2)
+    got = {m: gpu_rows(_run(m, qd, kd, vd, had), rows) for m in ("exact", "lean")}
+    kdq = oracle_dequant(*oracle_quant(k, had))
+    vdq = oracle_dequant(*oracle_quant(v, False))
+    qdq = np.zeros(q.shape, np.float32)
+    for j, (cq, sq) in fp8_quant_blocks_for_rows(q, rows, had).items():
+        qdq[:, j * 128:(j + 1) * 128] = oracle_dequant(cq, sq)
+    ref = sampled_rows_oracle(qdq, kdq, vdq, w.softmax_scale, rows)
+    n = np.linalg.norm(ref.ravel())
+    e = {m: float(np.linalg.norm((got[m] - ref).ravel()) / n) for m in got}
+    ratio = e["lean"] / e["exact"]
+    print(f"\nlean P {name} hadamard={had}: exact {e['exact']:.3e}, lean {e['lean']:.3e}, ratio {ratio:.2f}")
+    assert e["lean"] <= FP8_REL_L2
+    if max_ratio is not None:
+        assert ratio <= max_ratio
