@@ -129,10 +129,7 @@ struct Unit {
 // for each pair, the groups and then their query heads are adjacent. Units in
 // flight then share a few KV heads (K/V stay in L2) without every CTA
 // streaming the very same K/V tile at once.
-#ifndef ZYFA_GROUPS_IN_FLIGHT
-#define ZYFA_GROUPS_IN_FLIGHT 8
-#endif
-constexpr int kGroupsInFlight = ZYFA_GROUPS_IN_FLIGHT;
+constexpr int kGroupsInFlight = 8;
 
 __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles) {
   const int n_pairs = (n_qtiles + 1) / 2;
