@@ -65,6 +65,20 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8.restype = c_int
     L.zyfa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
                                     c_float, vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_bf16_rows.restype = c_int
+    L.zyfa_attn_fwd_bf16_rows.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                          vp, vp, vp, vp, c_int, c_int, vp]
+    L.zyfa_attn_fwd_fp8_rows.restype = c_int
+    L.zyfa_attn_fwd_fp8_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                                         c_float, vp, vp, vp, vp, c_int, c_int, vp]
+    L.zyfa_quantize_fp8_rows.restype = c_int
+    L.zyfa_quantize_fp8_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, c_int, c_int,
+                                         c_int, c_int, c_int, c_int, c_int, vp]
+    L.zyfa_prefill_fp8_host_workspace.restype = ctypes.c_size_t
+    L.zyfa_prefill_fp8_host_workspace.argtypes = [c_int] * 6
+    L.zyfa_prefill_fp8_host.restype = c_int
+    L.zyfa_prefill_fp8_host.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                        c_int, vp, ctypes.c_size_t, vp]
     L.zyfa_quantize_fp8_varlen.restype = c_int
     L.zyfa_quantize_fp8_varlen.argtypes = [vp, i64, i64, vp, vp, vp, c_int, c_int, c_int, c_int, vp]
     L.zyfa_attn_fwd_bf16_varlen.restype = c_int
@@ -113,9 +127,11 @@ def scale_blocks(S: int) -> int:
 
 def quantize_fp8(x: torch.Tensor, hadamard: bool = False, out: Optional[torch.Tensor] = None,
                  scales: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream: Optional[torch.cuda.Stream] = None,
+                 rows: Optional[Tuple[int, int]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Per-(b, h, 128-token block) e4m3 quantisation of a bf16 [B,S,H,D] tensor.
-    Returns (codes uint8 [B,S,H,D] dense, scales float32 [B,H,ceil(S/128)])."""
+    Returns (codes uint8 [B,S,H,D] dense, scales float32 [B,H,ceil(S/128)]).
+    rows=(begin, end): only the blocks covering those tokens are written."""
     _require(x, "x", torch.bfloat16)
     B, S, H, D = x.shape
     if out is None:
@@ -124,16 +140,23 @@ def quantize_fp8(x: torch.Tensor, hadamard: bool = False, out: Optional[torch.Te
         scales = torch.empty((B, H, scale_blocks(S)), dtype=torch.float32, device=x.device)
     if not out.is_contiguous() or not scales.is_contiguous():
         raise ValueError("out and scales must be contiguous")
-    _check(lib().zyfa_quantize_fp8(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), out.data_ptr(),
-                                   scales.data_ptr(), B, S, H, D, int(bool(hadamard)),
-                                   _stream_ptr(x, stream)))
+    if rows is None:
+        _check(lib().zyfa_quantize_fp8(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), out.data_ptr(),
+                                       scales.data_ptr(), B, S, H, D, int(bool(hadamard)),
+                                       _stream_ptr(x, stream)))
+    else:
+        _check(lib().zyfa_quantize_fp8_rows(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), out.data_ptr(),
+                                            scales.data_ptr(), B, S, H, D, int(bool(hadamard)), int(rows[0]),
+                                            int(rows[1]), _stream_ptr(x, stream)))
     return out, scales
 
 
 def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: Optional[float] = None,
                   out: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Causal attention on bf16 q [B,S,Hq,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv] -> o [B,S,Hq,Dv] bf16."""
+                  stream: Optional[torch.cuda.Stream] = None,
+                  rows: Optional[Tuple[int, int]] = None) -> torch.Tensor:
+    """Causal attention on bf16 q [B,S,Hq,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv] -> o [B,S,Hq,Dv] bf16.
+    rows=(begin, end): only those output rows (multiples of 256, or end = S)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _require(t, n, torch.bfloat16)
     B, S, Hq, Dqk = q.shape
@@ -143,17 +166,25 @@ def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_sca
     if out is None:
         out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     _require(out, "out", torch.bfloat16)
-    _check(lib().zyfa_attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
-                                    Dqk, Dv, float(softmax_scale), _strides(q), _strides(k), _strides(v),
-                                    _strides(out), _stream_ptr(q, stream)))
+    if rows is None:
+        _check(lib().zyfa_attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
+                                        Dqk, Dv, float(softmax_scale), _strides(q), _strides(k), _strides(v),
+                                        _strides(out), _stream_ptr(q, stream)))
+    else:
+        _check(lib().zyfa_attn_fwd_bf16_rows(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq,
+                                             Hkv, Dqk, Dv, float(softmax_scale), _strides(q), _strides(k),
+                                             _strides(v), _strides(out), int(rows[0]), int(rows[1]),
+                                             _stream_ptr(q, stream)))
     return out
 
 
 def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor,
                  v8: torch.Tensor, v_scale: torch.Tensor, softmax_scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Causal attention on per-block e4m3 inputs (uint8 codes + float32 block scales) -> bf16 o."""
+                 stream: Optional[torch.cuda.Stream] = None,
+                 rows: Optional[Tuple[int, int]] = None) -> torch.Tensor:
+    """Causal attention on per-block e4m3 inputs (uint8 codes + float32 block scales) -> bf16 o.
+    rows=(begin, end): only those output rows (multiples of 256, or end = S)."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
         _require(t, n, torch.uint8)
     for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
@@ -169,10 +200,16 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
     if out is None:
         out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
     _require(out, "out", torch.bfloat16)
-    _check(lib().zyfa_attn_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
-                                   v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk, Dv,
-                                   float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
-                                   _strides(out), _stream_ptr(q8, stream)))
+    if rows is None:
+        _check(lib().zyfa_attn_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                       v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk, Dv,
+                                       float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
+                                       _strides(out), _stream_ptr(q8, stream)))
+    else:
+        _check(lib().zyfa_attn_fwd_fp8_rows(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                            v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk,
+                                            Dv, float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
+                                            _strides(out), int(rows[0]), int(rows[1]), _stream_ptr(q8, stream)))
     return out
 
 
@@ -188,6 +225,41 @@ def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: boo
     v8, vs = quantize_fp8(v, False, stream=stream)
     o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream)
     return o, (q8, qs, k8, ks, v8, vs)
+
+
+def prefill_fp8_host_workspace(B: int, S: int, Hq: int, Hkv: int, Dqk: int, Dv: int,
+                               device=None) -> torch.Tensor:
+    """Device workspace (uint8) for prefill_fp8_host at these sizes."""
+    n = lib().zyfa_prefill_fp8_host_workspace(B, S, Hq, Hkv, Dqk, Dv)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def prefill_fp8_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
+                     softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                     n_chunks: int = 0, workspace: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The FP8 prefill on page-locked host tensors: copies in, quantisation,
+    attention and the copy of O back run as one pipeline along the sequence.
+    Returns the page-locked host o; it is valid once the stream (default: the
+    current one) has been synchronised."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or not t.is_pinned():
+            raise ValueError(f"{name} must be a dense, page-locked host bf16 tensor")
+    B, S, Hq, Dqk = q.shape
+    Hkv, Dv = k.shape[2], v.shape[3]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16).pin_memory()
+    if workspace is None:
+        workspace = prefill_fp8_host_workspace(B, S, Hq, Hkv, Dqk, Dv)
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    _check(lib().zyfa_prefill_fp8_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
+                                       Dqk, Dv, float(softmax_scale), int(bool(hadamard)), int(n_chunks),
+                                       workspace.data_ptr(), workspace.numel(), s.cuda_stream))
+    return out
 
 
 # ------------------------------------------------------ packed varlen batches

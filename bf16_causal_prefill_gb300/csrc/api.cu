@@ -181,10 +181,15 @@ int zyfa_set_fp8_probabilities(int mode) {
   return ZYFA_OK;
 }
 
-int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
-                      float* scales, int B, int S, int H, int D, int hadamard, void* stream) {
+static int quant_common(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                        float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
+                        void* stream) {
   if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
   if (B < 1 || S < 1 || H < 1) return fail(ZYFA_ERR_INVALID_ARG, "B, S, H must be >= 1");
+  if (row_begin < 0 || row_end > S || row_begin >= row_end || row_begin % 128 != 0 ||
+      (row_end != S && row_end % 128 != 0))
+    return fail(ZYFA_ERR_INVALID_ARG, "row range [%d, %d) must be non-empty, inside [0, %d), on 128-token blocks",
+                row_begin, row_end, S);
   if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
   if (hadamard && D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
   if (!aligned(x, 4) || !aligned(out, 2) || !aligned(scales, 4))
@@ -195,8 +200,23 @@ int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t
     return fail(ZYFA_ERR_INVALID_ARG, "grid too large");
   DeviceInfo* d;
   if (int r = device_info(&d)) return r;
-  zyfa::QuantArgs a{x, stride_b, stride_s, stride_h, static_cast<uint8_t*>(out), scales, B, S, H, D, hadamard,
-                    d->status, g_timeout_ns, d->sm_count};
+  zyfa::QuantArgs a{};
+  a.x = x;
+  a.sb = stride_b;
+  a.ss = stride_s;
+  a.sh = stride_h;
+  a.out = static_cast<uint8_t*>(out);
+  a.scales = scales;
+  a.B = B;
+  a.S = S;
+  a.H = H;
+  a.D = D;
+  a.blk_lo = row_begin / 128;
+  a.blk_hi = (row_end + 127) / 128;
+  a.hadamard = hadamard;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.num_sms = d->sm_count;
   cudaError_t e;
   // TMA streaming kernel when the input allows 16-byte tiled copies; the
   // register kernel otherwise. Both produce the same bytes.
@@ -223,13 +243,30 @@ int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t
   return ZYFA_OK;
 }
 
+int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                      float* scales, int B, int S, int H, int D, int hadamard, void* stream) {
+  return quant_common(x, stride_b, stride_s, stride_h, out, scales, B, S, H, D, hadamard, 0, S, stream);
+}
+
+int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                           float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
+                           void* stream) {
+  return quant_common(x, stride_b, stride_s, stride_h, out, scales, B, S, H, D, hadamard, row_begin, row_end,
+                      stream);
+}
+
 static int attn_common(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[3], const int64_t ks[3], const int64_t vs[3],
-                       const int64_t os[3], void* stream) {
+                       const int64_t os[3], int row_begin, int row_end, void* stream) {
   AttnCommon c{B, S, Hq, Hkv, Dqk, Dv, softmax_scale};
   const int elt = fp8 ? 1 : 2;
   if (int r = validate_attn(c, q, k, v, o, 16 / elt, qs, ks, vs, os)) return r;
+  if (row_begin < 0 || row_end > S || row_begin >= row_end || row_begin % 256 != 0 ||
+      (row_end % 256 != 0 && row_end != S))
+    return fail(ZYFA_ERR_INVALID_ARG,
+                "rows [%d, %d) must lie in [0, %d) with both ends multiples of 256 (or the end = S)", row_begin,
+                row_end, S);
   if (fp8) {
     if (!qsc || !ksc || !vsc) return fail(ZYFA_ERR_INVALID_ARG, "null scale pointer");
     if (!aligned(qsc, 4) || !aligned(ksc, 4) || !aligned(vsc, 4))
@@ -254,6 +291,8 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
   a.num_sms = d->sm_count;
   a.scale_blocks = (S + 127) / 128;
   a.lean_p = g_lean_p;
+  a.pair_lo = row_begin / 256;
+  a.pair_hi = (row_end + 255) / 256;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
@@ -264,7 +303,7 @@ int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int
                        int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                        const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
   return attn_common(false, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
-                     k_strides, v_strides, o_strides, stream);
+                     k_strides, v_strides, o_strides, 0, S, stream);
 }
 
 int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale, const void* v8,
@@ -272,7 +311,24 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
                       float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                       const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
   return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
-                     q_strides, k_strides, v_strides, o_strides, stream);
+                     q_strides, k_strides, v_strides, o_strides, 0, S, stream);
+}
+
+int zyfa_attn_fwd_bf16_rows(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                            int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
+                            const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
+                            int row_begin, int row_end, void* stream) {
+  return attn_common(false, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
+                     k_strides, v_strides, o_strides, row_begin, row_end, stream);
+}
+
+int zyfa_attn_fwd_fp8_rows(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                           const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                           int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                           const int64_t v_strides[3], const int64_t o_strides[3], int row_begin, int row_end,
+                           void* stream) {
+  return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, row_begin, row_end, stream);
 }
 
 // ----------------------------------------------------- packed varlen batches
@@ -396,8 +452,23 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
   if (T == 0) return ZYFA_OK;
   DeviceInfo* d;
   if (int r = device_info(&d)) return r;
-  zyfa::QuantArgs a{x, stride_t * T, stride_t, stride_h, static_cast<uint8_t*>(out), scales, 1, T, H, D, hadamard,
-                    d->status, g_timeout_ns, d->sm_count};
+  zyfa::QuantArgs a{};
+  a.x = x;
+  a.sb = stride_t * T;
+  a.ss = stride_t;
+  a.sh = stride_h;
+  a.out = static_cast<uint8_t*>(out);
+  a.scales = scales;
+  a.B = 1;
+  a.S = T;
+  a.H = H;
+  a.D = D;
+  a.blk_lo = 0;
+  a.blk_hi = (T + 127) / 128;
+  a.hadamard = hadamard;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.num_sms = d->sm_count;
   CUtensorMap tm;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 1};
   const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(stride_h) * 2, static_cast<cuuint64_t>(stride_t) * 2,
@@ -420,6 +491,186 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
   cudaError_t e = zyfa::launch_quantize_fp8_stream_varlen(tm, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
   return ZYFA_OK;
+}
+
+// ------------------------------------------------ prefill from host memory
+// Per-device copy streams and per-chunk events of the host pipeline.
+namespace {
+constexpr int kMaxChunks = 64;
+constexpr int kAttnStreams = 2;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr, att[kAttnStreams] = {};
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in[kMaxChunks] = {}, quant[kMaxChunks] = {}, done[kMaxChunks] = {};
+  std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ZYFA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  HostPipe& p = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!p.ready) {
+    const unsigned int ef = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&p.end, ef)) != cudaSuccess)
+      return fail_cuda(e, "host pipeline streams");
+    for (int i = 0; i < kAttnStreams; ++i)
+      if ((e = cudaStreamCreateWithFlags(&p.att[i], cudaStreamNonBlocking)) != cudaSuccess)
+        return fail_cuda(e, "host pipeline streams");
+    for (int i = 0; i < kMaxChunks; ++i)
+      if ((e = cudaEventCreateWithFlags(&p.in[i], ef)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&p.quant[i], ef)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&p.done[i], ef)) != cudaSuccess)
+        return fail_cuda(e, "host pipeline events");
+    p.ready = true;
+  }
+  *out = &p;
+  return ZYFA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace carve-up: bf16 staging of Q, K, V; their e4m3 codes and block
+// scales; the bf16 output before it goes back to the host.
+struct HostWorkspace {
+  size_t qd, kd, vd, q8, k8, v8, qs, ks, vs, od, total;
+};
+HostWorkspace host_workspace(int B, int S, int Hq, int Hkv, int Dqk, int Dv) {
+  const size_t tq = size_t(B) * S * Hq * Dqk, tk = size_t(B) * S * Hkv * Dqk, tv = size_t(B) * S * Hkv * Dv;
+  const size_t nb = size_t((S + 127) / 128);
+  HostWorkspace w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off += round256(bytes); return o; };
+  w.qd = take(tq * 2);
+  w.kd = take(tk * 2);
+  w.vd = take(tv * 2);
+  w.q8 = take(tq);
+  w.k8 = take(tk);
+  w.v8 = take(tv);
+  w.qs = take(size_t(B) * Hq * nb * 4);
+  w.ks = take(size_t(B) * Hkv * nb * 4);
+  w.vs = take(size_t(B) * Hkv * nb * 4);
+  w.od = take(size_t(B) * S * Hq * Dv * 2);
+  w.total = off;
+  return w;
+}
+
+bool page_locked(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+}  // namespace
+
+size_t zyfa_prefill_fp8_host_workspace(int B, int S, int Hq, int Hkv, int Dqk, int Dv) {
+  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;
+  return host_workspace(B, S, Hq, Hkv, Dqk, Dv).total;
+}
+
+int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                          int Dqk, int Dv, float softmax_scale, int hadamard, int n_chunks, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !workspace) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
+  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1)
+    return fail(ZYFA_ERR_INVALID_ARG, "B, S, Hq, Hkv must be >= 1 (got %d, %d, %d, %d)", B, S, Hq, Hkv);
+  if (n_chunks < 0 || n_chunks > kMaxChunks)
+    return fail(ZYFA_ERR_INVALID_ARG, "n_chunks = %d must be in [0, %d]", n_chunks, kMaxChunks);
+  if (!aligned(workspace, 256)) return fail(ZYFA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (!((Dqk == 128 && Dv == 128) || (Dqk == 192 && Dv == 128)))
+    return fail(ZYFA_ERR_UNSUPPORTED, "head dims (%d, %d) unsupported; use (128, 128) or (192, 128)", Dqk, Dv);
+  if (Hq % Hkv != 0) return fail(ZYFA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (hadamard && Dqk != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return fail(ZYFA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  const HostWorkspace w = host_workspace(B, S, Hq, Hkv, Dqk, Dv);
+  if (workspace_bytes < w.total)
+    return fail(ZYFA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                w.total);
+  if (!page_locked(q) || !page_locked(k) || !page_locked(v) || !page_locked(o))
+    return fail(ZYFA_ERR_INVALID_ARG, "q, k, v and o must be page-locked host memory");
+  HostPipe* p;
+  if (int r = host_pipe(&p)) return r;
+
+  // Chunk boundaries: multiples of 256 rows (attention pairs of query tiles).
+  const int pairs = (S + 255) / 256;
+  int n = n_chunks ? n_chunks : std::min(16, pairs);
+  n = std::max(1, std::min(n, pairs));
+  int bound[kMaxChunks + 1];
+  for (int c = 0; c <= n; ++c) bound[c] = std::min(S, static_cast<int>((static_cast<long long>(pairs) * c / n) * 256));
+  bound[n] = S;
+
+  char* ws = static_cast<char*>(workspace);
+  void *qd = ws + w.qd, *kd = ws + w.kd, *vd = ws + w.vd, *q8 = ws + w.q8, *k8 = ws + w.k8, *v8 = ws + w.v8;
+  float *qs = reinterpret_cast<float*>(ws + w.qs), *ks = reinterpret_cast<float*>(ws + w.ks),
+        *vs = reinterpret_cast<float*>(ws + w.vs);
+  void* od = ws + w.od;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t sq[3] = {int64_t(S) * Hq * Dqk, int64_t(Hq) * Dqk, Dqk};
+  const int64_t sk[3] = {int64_t(S) * Hkv * Dqk, int64_t(Hkv) * Dqk, Dqk};
+  const int64_t sv[3] = {int64_t(S) * Hkv * Dv, int64_t(Hkv) * Dv, Dv};
+  const int64_t so[3] = {int64_t(S) * Hq * Dv, int64_t(Hq) * Dv, Dv};
+
+  std::lock_guard<std::mutex> lock(p->mu);
+  cudaError_t e;
+  int rc = ZYFA_OK;
+  // Copy rows [r0, r1) of every batch of a dense [B,S,H,D] bf16 tensor.
+  auto copy_rows = [&](void* dst, const void* src, int64_t row_bytes, int r0, int r1, cudaMemcpyKind kind,
+                       cudaStream_t s) {
+    const size_t pitch = size_t(row_bytes) * S;
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + size_t(row_bytes) * r0, pitch,
+                             static_cast<const char*>(src) + size_t(row_bytes) * r0, pitch,
+                             size_t(row_bytes) * (r1 - r0), B, kind, s);
+  };
+  if ((e = cudaEventRecord(p->start, st)) != cudaSuccess) return fail_cuda(e, "cudaEventRecord");
+  if ((e = cudaStreamWaitEvent(p->h2d, p->start, 0)) != cudaSuccess) return fail_cuda(e, "cudaStreamWaitEvent");
+  for (int c = 0; c < n && rc == ZYFA_OK; ++c) {
+    const int r0 = bound[c], r1 = bound[c + 1];
+    if ((e = copy_rows(qd, q, int64_t(Hq) * Dqk * 2, r0, r1, cudaMemcpyHostToDevice, p->h2d)) != cudaSuccess ||
+        (e = copy_rows(kd, k, int64_t(Hkv) * Dqk * 2, r0, r1, cudaMemcpyHostToDevice, p->h2d)) != cudaSuccess ||
+        (e = copy_rows(vd, v, int64_t(Hkv) * Dv * 2, r0, r1, cudaMemcpyHostToDevice, p->h2d)) != cudaSuccess ||
+        (e = cudaEventRecord(p->in[c], p->h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, p->in[c], 0)) != cudaSuccess) {
+      rc = fail_cuda(e, "host pipeline: copy in");
+      break;
+    }
+    // Quantisers in order on the caller's stream; the attention of piece c on
+    // one of two streams, so that the next piece's attention can take the
+    // SMs that the tail of this one leaves idle (pieces depend only on the
+    // quantised inputs, never on each other's outputs).
+    cudaStream_t sa = p->att[c % kAttnStreams];
+    if ((rc = quant_common(qd, sq[0], sq[1], sq[2], q8, qs, B, S, Hq, Dqk, hadamard, r0, r1, stream)) ||
+        (rc = quant_common(kd, sk[0], sk[1], sk[2], k8, ks, B, S, Hkv, Dqk, hadamard, r0, r1, stream)) ||
+        (rc = quant_common(vd, sv[0], sv[1], sv[2], v8, vs, B, S, Hkv, Dv, 0, r0, r1, stream)))
+      break;
+    if ((e = cudaEventRecord(p->quant[c], st)) != cudaSuccess || (e = cudaStreamWaitEvent(sa, p->quant[c], 0)) != cudaSuccess) {
+      rc = fail_cuda(e, "host pipeline: order attention");
+      break;
+    }
+    if ((rc = attn_common(true, q8, qs, k8, ks, v8, vs, od, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, sq, sk, sv, so,
+                          r0, r1, sa)))
+      break;
+    if ((e = cudaEventRecord(p->done[c], sa)) != cudaSuccess || (e = cudaStreamWaitEvent(p->d2h, p->done[c], 0)) != cudaSuccess ||
+        (e = copy_rows(o, od, int64_t(Hq) * Dv * 2, r0, r1, cudaMemcpyDeviceToHost, p->d2h)) != cudaSuccess)
+      rc = fail_cuda(e, "host pipeline: copy out");
+  }
+  // Join both copy streams back into the caller's stream, also on error, so
+  // that nothing of this call is left unordered against the caller's work.
+  cudaStream_t side[2 + kAttnStreams] = {p->h2d, p->d2h};
+  for (int i = 0; i < kAttnStreams; ++i) side[2 + i] = p->att[i];
+  for (cudaStream_t x : side)
+    if ((e = cudaEventRecord(p->end, x)) != cudaSuccess || (e = cudaStreamWaitEvent(st, p->end, 0)) != cudaSuccess)
+      if (rc == ZYFA_OK) rc = fail_cuda(e, "host pipeline: join");
+  return rc;
 }
 
 int zyfa_get_device_status(void* stream, unsigned int* word) {

@@ -131,8 +131,9 @@ struct Unit {
 // streaming the very same K/V tile at once.
 constexpr int kGroupsInFlight = 8;
 
-__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles) {
-  const int n_pairs = (n_qtiles + 1) / 2;
+// Pairs pair_lo .. pair_hi - 1 only (a row range of a chunked prefill).
+__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles, int pair_lo, int pair_hi) {
+  const int n_pairs = pair_hi - pair_lo;
   const int G = Hq / Hkv;
   const int n_groups = B * Hkv;
   const int per_sg = kGroupsInFlight * G * n_pairs;
@@ -147,7 +148,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
   Unit w;
   w.b = group / Hkv;
   const int hkv = group - w.b * Hkv;
-  w.t = n_pairs - 1 - tq;
+  w.t = pair_hi - 1 - tq;
   w.hq = hkv * G + (rr - gi * G);
   w.has_b = (2 * w.t + 1) < n_qtiles;
   w.n_a = 2 * w.t + 1;
@@ -166,10 +167,10 @@ template <bool VARLEN>
 struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
-  int B, Hq, Hkv, S, n_qtiles;
+  int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
   __device__ __forceinline__ int n_units() const {
     if constexpr (VARLEN) return tab->level_start[tab->n_levels];
-    else return B * Hq * ((n_qtiles + 1) / 2);
+    else return B * Hq * (pair_hi - pair_lo);
   }
   __device__ __forceinline__ Unit decode(int u) const {
     if constexpr (VARLEN) {
@@ -195,7 +196,7 @@ struct Sched {
       w.n_kv = w.has_b ? w.n_b : w.n_a;
       return w;
     } else {
-      Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles);
+      Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles, pair_lo, pair_hi);
       w.len = S;
       return w;
     }
@@ -825,6 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.Hkv = a.Hkv;
   sc.S = a.S;
   sc.n_qtiles = (a.S + 127) / 128;
+  sc.pair_lo = a.pair_lo;
+  sc.pair_hi = a.pair_hi;
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
@@ -892,8 +895,7 @@ cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUten
 }
 
 long long fixed_units(const AttnArgs& a) {
-  const int n_qtiles = (a.S + 127) / 128;
-  return static_cast<long long>(a.B) * a.Hq * ((n_qtiles + 1) / 2);
+  return static_cast<long long>(a.B) * a.Hq * (a.pair_hi - a.pair_lo);
 }
 
 }  // namespace

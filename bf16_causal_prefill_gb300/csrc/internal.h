@@ -19,6 +19,7 @@ struct QuantArgs {
   uint8_t* out;           // e4m3 [B,S,H,D] dense
   float* scales;          // [B,H,ceil(S/128)]
   int B, S, H, D;
+  int blk_lo, blk_hi;     // 128-token blocks processed: [blk_lo, blk_hi) of ceil(S/128)
   int hadamard;
   unsigned int* status;   // device status word (streaming kernel's bounded waits)
   uint64_t timeout_ns;
@@ -75,6 +76,7 @@ struct AttnArgs {
   int num_sms;
   int scale_blocks;        // fp8: blocks per (sequence, head) row of the scale arrays
   int lean_p;              // fp8, head dim 128: lean P instead of exact P
+  int pair_lo, pair_hi;    // equal lengths: only query-tile pairs [pair_lo, pair_hi) (rows 256*lo .. 256*hi)
 };
 
 // tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of

@@ -55,9 +55,9 @@ template <int D, bool kHadamard>
 __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(QuantArgs a) {
   constexpr int kPairs = D / 64;   // bf16 pairs per lane per row
   static_assert(!kHadamard || D == 128, "rotation is defined for head dim 128");
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int blk = a.blk_lo + blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nblk = gridDim.x;
+  const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
 
   float v[kRowsPerWarp][2 * kPairs];
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
   long long total;
   if constexpr (VARLEN) total = static_cast<long long>(a.H) * tab.cum_blocks[tab.n_seqs];
-  else total = static_cast<long long>(a.B) * a.H * nblk;
+  else total = static_cast<long long>(a.B) * a.H * (a.blk_hi - a.blk_lo);
   const long long first = blockIdx.x, step = gridDim.x;
 
   // Equal lengths: blocks in (b, h, blk) order. Packed sequences: sequence
@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       q.valid = min(kBlockTokens, tab.len[lo] - blk * kBlockTokens);
       q.scale_idx = (static_cast<int64_t>(lo) * a.H + q.h) * tab.max_blocks + blk;
     } else {
-      const int blk = static_cast<int>(g % nblk);
-      const long long bh = g / nblk;
+      const int range = a.blk_hi - a.blk_lo;
+      const int blk = a.blk_lo + static_cast<int>(g % range);
+      const long long bh = g / range;
       q.h = static_cast<int>(bh % a.H);
       q.b = static_cast<int>(bh / a.H);
       q.tok = blk * kBlockTokens;
@@ -348,8 +349,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 }  // namespace
 
 cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
-  const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
-  dim3 grid(nblk, a.H, a.B);
+  if (a.blk_hi <= a.blk_lo) return cudaSuccess;
+  dim3 grid(a.blk_hi - a.blk_lo, a.H, a.B);
   if (a.D == 128 && a.hadamard) {
     quantize_fp8_kernel<128, true><<<grid, kQuantThreads, 0, stream>>>(a);
   } else if (a.D == 128) {
@@ -376,7 +377,7 @@ static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, co
 
 cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream) {
   const NoQuantTable none{};
-  const long long total = static_cast<long long>(a.B) * a.H * ((a.S + kBlockTokens - 1) / kBlockTokens);
+  const long long total = static_cast<long long>(a.B) * a.H * (a.blk_hi - a.blk_lo);
   if (a.D == 128 && a.hadamard) return launch_stream<128, true, false>(tm_x, a, none, total, stream);
   if (a.D == 128) return launch_stream<128, false, false>(tm_x, a, none, total, stream);
   if (a.D == 192) return launch_stream<192, false, false>(tm_x, a, none, total, stream);

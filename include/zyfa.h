@@ -36,6 +36,7 @@
 #ifndef ZYFA_H_
 #define ZYFA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -85,6 +86,19 @@ int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t
                       float* scales, int B, int S, int H, int D, int hadamard, void* stream);
 
 /*
+ * Row-range form of zyfa_quantize_fp8: only the 128-token blocks covering
+ * tokens [row_begin, row_end) of every (batch, head) are read, quantised and
+ * written (their codes into out and their scales into scales, both the
+ * full-size [B,S,H,D] / [B,H,ceil(S/128)] arrays); everything else is left
+ * untouched. row_begin is a multiple of 128, row_end a multiple of 128 or S,
+ * 0 <= row_begin < row_end <= S. The bytes written equal those of the full
+ * call, so a tensor arriving in pieces can be quantised piece by piece.
+ */
+int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                           float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
+                           void* stream);
+
+/*
  * Causal attention, BF16 in and out ("ZYFA ..." Introduction; grouped-query
  * heads: query head h reads KV head h / (Hq / Hkv)):
  *   O[b,i,h,:] = sum_{j<=i} softmax_j(softmax_scale * Q[b,i,h].K[b,j,g]) V[b,j,g]
@@ -127,6 +141,54 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
                       const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                       int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                       const int64_t v_strides[3], const int64_t o_strides[3], void* stream);
+
+/*
+ * Row-range ("chunked prefill") forms of the two calls above: only output rows
+ * [row_begin, row_end) of every (batch, head) are computed and written, each
+ * attending causally to keys 0..row (so K and V are read for rows
+ * [0, row_end) only; Q only for the range). row_begin and row_end are
+ * multiples of 256, or row_end = S; 0 <= row_begin < row_end <= S. Results
+ * are bitwise equal to the same rows of the full call, so a prefill can be
+ * split along the sequence and overlapped with the copies of its inputs.
+ * Other arguments and errors as the full calls.
+ */
+int zyfa_attn_fwd_bf16_rows(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                            int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
+                            const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
+                            int row_begin, int row_end, void* stream);
+int zyfa_attn_fwd_fp8_rows(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                           const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                           int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                           const int64_t v_strides[3], const int64_t o_strides[3], int row_begin, int row_end,
+                           void* stream);
+
+/*
+ * The FP8 prefill from host memory: Q, K, V go to the device, are quantised
+ * (zyfa_quantize_fp8, with the rotation when hadamard != 0, V never rotated),
+ * attended (zyfa_attn_fwd_fp8) and O comes back, in n_chunks pieces along the
+ * sequence, so that the copy of piece c+1 in and of piece c-1 out overlap the
+ * kernels of piece c. Pieces are whole multiples of 256 rows (the last one
+ * may be shorter); n_chunks = 0 picks min(16, ceil(S/256)). The bytes of o
+ * equal those of the device-resident calls on the same inputs.
+ *
+ * q, k, v : bf16 [B,S,Hq,Dqk], [B,S,Hkv,Dqk], [B,S,Hkv,Dv], dense, in
+ *           page-locked host memory; o: bf16 [B,S,Hq,Dv] dense, page-locked.
+ * workspace : device memory of at least zyfa_prefill_fp8_host_workspace()
+ *           bytes, 256-byte aligned, owned by the caller, not used by anything
+ *           else until the call's work has finished.
+ * stream  : the call orders itself after the work already on stream and
+ *           before work queued on it later (it uses streams of its
+ *           own in between); o is valid once stream has been synchronised.
+ *           The call itself returns once everything is queued.
+ * Errors  : as zyfa_attn_fwd_fp8; ZYFA_ERR_INVALID_ARG for pageable host
+ *           buffers or a short workspace. After an error the queued part of
+ *           the work is still ordered before later work on stream, and o is
+ *           unspecified.
+ */
+size_t zyfa_prefill_fp8_host_workspace(int B, int S, int Hq, int Hkv, int Dqk, int Dv);
+int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                          int Dqk, int Dv, float softmax_scale, int hadamard, int n_chunks, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /*
  * Packed variable-length batches. The pages time equal-length batches and

@@ -134,3 +134,61 @@ def test_varlen_quantiser_rejects_bad_arguments_on_host(L):
     assert q(16, 132, 128, 16, 16, _cu(0, 4), 1, 1, 128, 0, None) == 2        # token stride not a multiple of 8
     assert q(8, 128, 128, 16, 16, _cu(0, 4), 1, 1, 128, 0, None) == 2         # base not 16-byte aligned
     assert q(16, 128, 128, 16, 16, _cu(0, 0), 1, 1, 128, 0, None) == 0        # empty: nothing enqueued
+
+
+def _rows(L, fp8, r0, r1, S=1000):
+    st = (I3(S * 256, 256, 128), I3(S * 128, 128, 128), I3(S * 128, 128, 128), I3(S * 256, 256, 128))
+    if fp8:
+        return L.zyfa_attn_fwd_fp8_rows(16, 16, 16, 16, 16, 16, 16, 1, S, 2, 1, 128, 128, ctypes.c_float(0.1),
+                                        *st, r0, r1, None)
+    return L.zyfa_attn_fwd_bf16_rows(16, 16, 16, 16, 1, S, 2, 1, 128, 128, ctypes.c_float(0.1), *st, r0, r1, None)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("r0,r1", [(-256, 256), (0, 0), (256, 256), (512, 256), (128, 512), (0, 300),
+                                   (0, 1001), (768, 1200)])
+def test_row_range_attention_rejects_bad_ranges_on_host(L, fp8, r0, r1):
+    # ranges are non-empty, inside [0, S), and on 256-row boundaries (or end at S)
+    assert _rows(L, fp8, r0, r1) == 1
+    assert "rows" in L.zyfa_last_error_message().decode()
+
+
+def test_row_range_quantiser_rejects_bad_ranges_on_host(L):
+    q = L.zyfa_quantize_fp8_rows
+    for r0, r1 in ((-128, 128), (0, 0), (64, 256), (0, 200), (0, 1001), (256, 128)):
+        assert q(16, 1000 * 128, 128, 128, 16, 16, 1, 1000, 1, 128, 0, r0, r1, None) == 1, (r0, r1)
+
+
+def test_host_prefill_workspace_size(L):
+    B, S, Hq, Hkv, D = 2, 1000, 4, 2, 128
+    r = lambda n: (n + 255) // 256 * 256
+    tq, tk = B * S * Hq * D, B * S * Hkv * D
+    nb = (S + 127) // 128
+    want = r(2 * tq) + 2 * r(2 * tk) + r(tq) + 2 * r(tk) + r(4 * B * Hq * nb) \
+        + 2 * r(4 * B * Hkv * nb) + r(2 * tq)
+    assert L.zyfa_prefill_fp8_host_workspace(B, S, Hq, Hkv, D, D) == want
+    assert L.zyfa_prefill_fp8_host_workspace(0, S, Hq, Hkv, D, D) == 0
+
+
+def test_host_prefill_rejects_bad_arguments_on_host(L):
+    p = L.zyfa_prefill_fp8_host
+    n = L.zyfa_prefill_fp8_host_workspace(1, 512, 2, 1, 128, 128)
+    ok = dict(q=16, k=16, v=16, o=16, Dqk=128, Dv=128, Hq=2, Hkv=1, scale=0.1, had=0, chunks=0, ws=256, wsn=n)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return p(a["q"], a["k"], a["v"], a["o"], 1, 512, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"],
+                 ctypes.c_float(a["scale"]), a["had"], a["chunks"], a["ws"], a["wsn"], None)
+
+    assert call(q=0) == 1                     # null pointer
+    assert call(ws=0) == 1                    # no workspace
+    assert call(ws=128) == 1                  # workspace not 256-byte aligned
+    assert call(wsn=n - 1) == 1               # workspace too small
+    assert call(chunks=-1) == 1
+    assert call(chunks=65) == 1
+    assert call(Dqk=64, Dv=64) == 2
+    assert call(Hq=3, Hkv=2) == 1
+    assert call(Dqk=192, had=1) == 2          # rotation needs head dim 128
+    assert call(scale=0.0) == 1
+    assert call() == 1                        # host buffers are not page-locked
+    assert "page-locked" in L.zyfa_last_error_message().decode()
