@@ -79,6 +79,17 @@ def lib() -> ctypes.CDLL:
     L.zyfa_prefill_fp8_host.restype = c_int
     L.zyfa_prefill_fp8_host.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                                         c_int, vp, ctypes.c_size_t, vp]
+    L.zyfa_varlen_workspace_bytes.restype = ctypes.c_size_t
+    L.zyfa_varlen_workspace_bytes.argtypes = []
+    L.zyfa_quantize_fp8_varlen_dev.restype = c_int
+    L.zyfa_quantize_fp8_varlen_dev.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, c_int, c_int, c_int,
+                                               c_int, c_int, c_int, vp, vp]
+    L.zyfa_attn_fwd_bf16_varlen_dev.restype = c_int
+    L.zyfa_attn_fwd_bf16_varlen_dev.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                                c_float, vp, vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_fp8_varlen_dev.restype = c_int
+    L.zyfa_attn_fwd_fp8_varlen_dev.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                               c_int, c_int, c_float, vp, vp, vp, vp, vp, vp]
     L.zyfa_quantize_fp8_varlen.restype = c_int
     L.zyfa_quantize_fp8_varlen.argtypes = [vp, i64, i64, vp, vp, vp, c_int, c_int, c_int, c_int, vp]
     L.zyfa_attn_fwd_bf16_varlen.restype = c_int
@@ -278,6 +289,28 @@ def _cu_host(cu_seqlens) -> Tuple[ctypes.Array, int, int]:
     return arr, len(vals) - 1, max_len
 
 
+def _cu_device(cu_seqlens, max_seqlen: Optional[int], device) -> Optional[Tuple[int, int, int]]:
+    """(pointer, B, max_seqlen) when cu_seqlens is an int32 CUDA tensor and the
+    caller gave max_seqlen: the offsets stay on the device (no host read, no
+    synchronisation). None otherwise (the host path)."""
+    if max_seqlen is None or not isinstance(cu_seqlens, torch.Tensor) or not cu_seqlens.is_cuda:
+        return None
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("device cu_seqlens must be a contiguous 1-D int32 CUDA tensor")
+    if cu_seqlens.device != device:
+        raise ValueError("cu_seqlens must be on the same device as the tensors")
+    if cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens needs at least two entries")
+    return cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(max_seqlen)
+
+
+def _varlen_workspace(device, stream: Optional[torch.cuda.Stream]) -> torch.Tensor:
+    ws = torch.empty(lib().zyfa_varlen_workspace_bytes(), dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)
+    return ws
+
+
 def _require_packed(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -296,14 +329,25 @@ def _strides2(t: torch.Tensor):
 
 
 def quantize_fp8_varlen(x: torch.Tensor, cu_seqlens, hadamard: bool = False,
-                        stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                        stream: Optional[torch.cuda.Stream] = None,
+                        max_seqlen: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Per-(sequence, head, 128-token block) e4m3 quantisation of a packed bf16
     [T,H,D] tensor. Returns (codes uint8 [T,H,D], scales float32
-    [B,H,ceil(max_len/128)])."""
+    [B,H,ceil(max_len/128)]). An int32 CUDA cu_seqlens with max_seqlen given
+    stays on the device (scales then [B,H,ceil(max_seqlen/128)])."""
     _require_packed(x, "x", torch.bfloat16)
     T, H, D = x.shape
-    cu, B, max_len = _cu_host(cu_seqlens)
     out = torch.empty((T, H, D), dtype=torch.uint8, device=x.device)
+    dev = _cu_device(cu_seqlens, max_seqlen, x.device)
+    if dev is not None:
+        cu_ptr, B, max_len = dev
+        scales = torch.zeros((B, H, scale_blocks(max_len)), dtype=torch.float32, device=x.device)
+        ws = _varlen_workspace(x.device, stream)
+        _check(lib().zyfa_quantize_fp8_varlen_dev(x.data_ptr(), x.stride(0), x.stride(1), out.data_ptr(),
+                                                  scales.data_ptr(), cu_ptr, B, T, max_len, H, D,
+                                                  int(bool(hadamard)), ws.data_ptr(), _stream_ptr(x, stream)))
+        return out, scales
+    cu, B, max_len = _cu_host(cu_seqlens)
     scales = torch.zeros((B, H, scale_blocks(max_len)), dtype=torch.float32, device=x.device)
     _check(lib().zyfa_quantize_fp8_varlen(x.data_ptr(), x.stride(0), x.stride(1), out.data_ptr(), scales.data_ptr(),
                                           cu, B, H, D, int(bool(hadamard)), _stream_ptr(x, stream)))
@@ -312,20 +356,31 @@ def quantize_fp8_varlen(x: torch.Tensor, cu_seqlens, hadamard: bool = False,
 
 def attn_fwd_bf16_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens,
                          softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                         stream: Optional[torch.cuda.Stream] = None,
+                         max_seqlen: Optional[int] = None) -> torch.Tensor:
     """Causal attention over a packed variable-length batch: q [T,Hq,Dqk],
     k [T,Hkv,Dqk], v [T,Hkv,Dv] -> o [T,Hq,Dv] bf16; each sequence attends to
-    itself only."""
+    itself only. An int32 CUDA cu_seqlens with max_seqlen given stays on the
+    device."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _require_packed(t, n, torch.bfloat16)
     T, Hq, Dqk = q.shape
     Hkv, Dv = k.shape[1], v.shape[2]
-    cu, B, _ = _cu_host(cu_seqlens)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(Dqk)
     if out is None:
         out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     _require_packed(out, "out", torch.bfloat16)
+    dev = _cu_device(cu_seqlens, max_seqlen, q.device)
+    if dev is not None:
+        cu_ptr, B, max_len = dev
+        ws = _varlen_workspace(q.device, stream)
+        _check(lib().zyfa_attn_fwd_bf16_varlen_dev(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), cu_ptr,
+                                                   B, T, max_len, Hq, Hkv, Dqk, Dv, float(softmax_scale),
+                                                   _strides2(q), _strides2(k), _strides2(v), _strides2(out),
+                                                   ws.data_ptr(), _stream_ptr(q, stream)))
+        return out
+    cu, B, _ = _cu_host(cu_seqlens)
     _check(lib().zyfa_attn_fwd_bf16_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), cu, B, Hq,
                                            Hkv, Dqk, Dv, float(softmax_scale), _strides2(q), _strides2(k),
                                            _strides2(v), _strides2(out), _stream_ptr(q, stream)))
@@ -335,14 +390,21 @@ def attn_fwd_bf16_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_s
 def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor,
                         v8: torch.Tensor, v_scale: torch.Tensor, cu_seqlens, softmax_scale: Optional[float] = None,
                         out: Optional[torch.Tensor] = None,
-                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                        stream: Optional[torch.cuda.Stream] = None,
+                        max_seqlen: Optional[int] = None) -> torch.Tensor:
     """FP8 causal attention over a packed variable-length batch (codes and
-    scales as written by quantize_fp8_varlen) -> bf16 o [T,Hq,Dv]."""
+    scales as written by quantize_fp8_varlen) -> bf16 o [T,Hq,Dv]. An int32
+    CUDA cu_seqlens with max_seqlen given stays on the device."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
         _require_packed(t, n, torch.uint8)
     T, Hq, Dqk = q8.shape
     Hkv, Dv = k8.shape[1], v8.shape[2]
-    cu, B, max_len = _cu_host(cu_seqlens)
+    dev = _cu_device(cu_seqlens, max_seqlen, q8.device)
+    if dev is not None:
+        cu_ptr, B, max_len = dev
+        cu = None
+    else:
+        cu, B, max_len = _cu_host(cu_seqlens)
     nb = scale_blocks(max_len)
     for t, n, h in ((q_scale, "q_scale", Hq), (k_scale, "k_scale", Hkv), (v_scale, "v_scale", Hkv)):
         if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, h, nb):
@@ -352,6 +414,14 @@ def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
     if out is None:
         out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
     _require_packed(out, "out", torch.bfloat16)
+    if dev is not None:
+        ws = _varlen_workspace(q8.device, stream)
+        _check(lib().zyfa_attn_fwd_fp8_varlen_dev(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(),
+                                                  k_scale.data_ptr(), v8.data_ptr(), v_scale.data_ptr(),
+                                                  out.data_ptr(), cu_ptr, B, T, max_len, Hq, Hkv, Dqk, Dv,
+                                                  float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
+                                                  _strides2(out), ws.data_ptr(), _stream_ptr(q8, stream)))
+        return out
     _check(lib().zyfa_attn_fwd_fp8_varlen(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
                                           v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, B, Hq, Hkv, Dqk,
                                           Dv, float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
@@ -360,15 +430,16 @@ def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
 
 
 def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens, hadamard: bool = False,
-                       softmax_scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None):
+                       softmax_scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None,
+                       max_seqlen: Optional[int] = None):
     """The FP8 prefill path over a packed variable-length batch. Returns
     (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[2])
-    q8, qs = quantize_fp8_varlen(q, cu_seqlens, hadamard, stream=stream)
-    k8, ks = quantize_fp8_varlen(k, cu_seqlens, hadamard, stream=stream)
-    v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream)
-    o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream)
+    q8, qs = quantize_fp8_varlen(q, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
+    k8, ks = quantize_fp8_varlen(k, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
+    v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream, max_seqlen=max_seqlen)
+    o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream, max_seqlen=max_seqlen)
     return o, (q8, qs, k8, ks, v8, vs)
 
 

@@ -350,12 +350,38 @@ static int read_seqlens(const int32_t* cu, int B, int* total, int* max_len) {
   return ZYFA_OK;
 }
 
+// Device-resident offsets: the caller states the packed token count and an
+// upper bound on the sequence length; the tables are built on the device into
+// the caller's workspace ([SeqTable][QuantSeqTable], 256-byte aligned).
+static size_t varlen_ws_quant_offset() { return (sizeof(zyfa::SeqTable) + 255) & ~size_t(255); }
+static size_t varlen_ws_bytes() { return varlen_ws_quant_offset() + ((sizeof(zyfa::QuantSeqTable) + 255) & ~size_t(255)); }
+
+static int check_dev_seqlens(const int32_t* cu, int B, int total, int max_len, void* workspace) {
+  if (!cu) return fail(ZYFA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (B < 1 || B > zyfa::kMaxVarlenSeqs)
+    return fail(ZYFA_ERR_INVALID_ARG, "batch %d outside 1..%d", B, zyfa::kMaxVarlenSeqs);
+  if (total < 0) return fail(ZYFA_ERR_INVALID_ARG, "total_tokens must be >= 0");
+  if (max_len < 0) return fail(ZYFA_ERR_INVALID_ARG, "max_seqlen must be >= 0");
+  if (max_len > 2 * 128 * zyfa::kMaxVarlenLevels)
+    return fail(ZYFA_ERR_UNSUPPORTED, "max_seqlen %d exceeds %d", max_len, 2 * 128 * zyfa::kMaxVarlenLevels);
+  if (!workspace || !aligned(workspace, 256)) return fail(ZYFA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (!aligned(cu, 4)) return fail(ZYFA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+  return ZYFA_OK;
+}
+
 static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, const int32_t* cu, int B, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[2], const int64_t ks[2], const int64_t vs[2],
-                       const int64_t os[2], void* stream) {
+                       const int64_t os[2], void* stream, const int32_t* cu_dev = nullptr, int total_dev = 0,
+                       int max_len_dev = 0, void* workspace = nullptr) {
   int T = 0, max_len = 0;
-  if (int r = read_seqlens(cu, B, &T, &max_len)) return r;
+  if (cu_dev) {
+    if (int r = check_dev_seqlens(cu_dev, B, total_dev, max_len_dev, workspace)) return r;
+    T = total_dev;
+    max_len = max_len_dev;
+  } else if (int r = read_seqlens(cu, B, &T, &max_len)) {
+    return r;
+  }
   if (!qs || !ks || !vs || !os) return fail(ZYFA_ERR_INVALID_ARG, "strides pointer is null");
   if (T == 0) return ZYFA_OK;   // nothing to compute
   // The packed tensors as one batch of T tokens.
@@ -377,6 +403,27 @@ static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k,
   if ((r = make_map(&tq, q, dt, elt, Dqk, Hq, T, 1, q3, "q")) || (r = make_map(&tk, k, dt, elt, Dqk, Hkv, T, 1, k3, "k")) ||
       (r = make_map(&tv, v, dt, elt, Dv, Hkv, T, 1, v3, "v")))
     return r;
+  zyfa::AttnArgs a{};
+  a.B = 1; a.S = T; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o; a.o_sb = o3[0]; a.o_ss = o3[1]; a.o_sh = o3[2];
+  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.debug_stall = g_debug_stall;
+  a.num_sms = d->sm_count;
+  a.scale_blocks = (max_len + 127) / 128;
+  a.lean_p = g_lean_p;
+  if (cu_dev) {
+    auto* dtab = static_cast<zyfa::SeqTable*>(workspace);
+    cudaError_t e = zyfa::launch_build_seq_tables(cu_dev, B, T, max_len, Hq, dtab, nullptr, d->status,
+                                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "build_seq_tables launch");
+    e = fp8 ? zyfa::launch_attn_fp8_varlen_dev(tq, tk, tv, a, dtab, static_cast<cudaStream_t>(stream))
+            : zyfa::launch_attn_bf16_varlen_dev(tq, tk, tv, a, dtab, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");
+    return ZYFA_OK;
+  }
   // Unit table: non-empty sequences, longest first; level k holds pair
   // t = n_levels - 1 - k of every sequence with more than t pairs.
   static thread_local zyfa::SeqTable tab;
@@ -403,17 +450,6 @@ static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k,
   tab.level_start[0] = 0;
   for (int kl = 0; kl < tab.n_levels; ++kl)
     tab.level_start[kl + 1] = tab.level_start[kl] + cnt[tab.n_levels - 1 - kl] * Hq;
-  zyfa::AttnArgs a{};
-  a.B = 1; a.S = T; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
-  a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  a.o = o; a.o_sb = o3[0]; a.o_ss = o3[1]; a.o_sh = o3[2];
-  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
-  a.status = d->status;
-  a.timeout_ns = g_timeout_ns;
-  a.debug_stall = g_debug_stall;
-  a.num_sms = d->sm_count;
-  a.scale_blocks = (max_len + 127) / 128;
-  a.lean_p = g_lean_p;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");
@@ -437,10 +473,18 @@ int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k
                      q_strides, k_strides, v_strides, o_strides, stream);
 }
 
-int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
-                             const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream) {
+static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                        const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream,
+                        const int32_t* cu_dev = nullptr, int total_dev = 0, int max_len_dev = 0,
+                        void* workspace = nullptr) {
   int T = 0, max_len = 0;
-  if (int r = read_seqlens(cu_seqlens, B, &T, &max_len)) return r;
+  if (cu_dev) {
+    if (int r = check_dev_seqlens(cu_dev, B, total_dev, max_len_dev, workspace)) return r;
+    T = total_dev;
+    max_len = max_len_dev;
+  } else if (int r = read_seqlens(cu_seqlens, B, &T, &max_len)) {
+    return r;
+  }
   if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
   if (H < 1 || H > 65535) return fail(ZYFA_ERR_INVALID_ARG, "H must be in 1..65535");
   if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
@@ -479,6 +523,15 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(x) failed: %d", (int)cr);
+  if (cu_dev) {
+    auto* dtab = reinterpret_cast<zyfa::QuantSeqTable*>(static_cast<char*>(workspace) + varlen_ws_quant_offset());
+    cudaError_t e = zyfa::launch_build_seq_tables(cu_dev, B, T, max_len, H, nullptr, dtab, d->status,
+                                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "build_seq_tables launch");
+    e = zyfa::launch_quantize_fp8_stream_varlen_dev(tm, a, dtab, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
+    return ZYFA_OK;
+  }
   static thread_local zyfa::QuantSeqTable tab;
   tab.n_seqs = B;
   tab.max_blocks = (max_len + 127) / 128;
@@ -491,6 +544,41 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
   cudaError_t e = zyfa::launch_quantize_fp8_stream_varlen(tm, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
   return ZYFA_OK;
+}
+
+int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                             const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream) {
+  return quant_varlen(x, stride_t, stride_h, out, scales, cu_seqlens, B, H, D, hadamard, stream);
+}
+
+size_t zyfa_varlen_workspace_bytes(void) { return varlen_ws_bytes(); }
+
+int zyfa_quantize_fp8_varlen_dev(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                                 const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen, int H, int D,
+                                 int hadamard, void* workspace, void* stream) {
+  return quant_varlen(x, stride_t, stride_h, out, scales, nullptr, B, H, D, hadamard, stream, cu_seqlens_dev,
+                      total_tokens, max_seqlen, workspace);
+}
+
+int zyfa_attn_fwd_bf16_varlen_dev(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens_dev,
+                                  int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
+                                  float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
+                                  const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
+                                  void* stream) {
+  return attn_varlen(false, q, nullptr, k, nullptr, v, nullptr, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
+                     workspace);
+}
+
+int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                                 const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens_dev, int B,
+                                 int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
+                                 float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
+                                 const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
+                                 void* stream) {
+  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
+                     workspace);
 }
 
 // ------------------------------------------------ prefill from host memory
@@ -685,7 +773,9 @@ int zyfa_get_device_status(void* stream, unsigned int* word) {
   if ((e = cudaMemcpyToSymbol(zyfa_device_status_word, &zero, sizeof(zero))) != cudaSuccess)
     return fail_cuda(e, "clear status word");
   if (word) *word = w;
-  if (w) return fail(ZYFA_ERR_TIMEOUT, "device status word 0x%x: a kernel wait timed out", w);
+  if (w & ~zyfa::kStatusBadSeqlens) return fail(ZYFA_ERR_TIMEOUT, "device status word 0x%x: a kernel wait timed out", w);
+  if (w) return fail(ZYFA_ERR_INVALID_ARG, "device status word 0x%x: device cu_seqlens were not a valid partition "
+                     "(nothing was computed for that call)", w);
   return ZYFA_OK;
 }
 

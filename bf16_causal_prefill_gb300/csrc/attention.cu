@@ -834,7 +834,8 @@ template <int DQK, bool FP8, bool VARLEN, bool LEAN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
-                    const __grid_constant__ typename Sched<VARLEN>::Table tab) {
+                    const __grid_constant__ typename Sched<VARLEN>::Table tab,
+                    const typename Sched<VARLEN>::Table* tab_global) {
   using C = Cfg<DQK, FP8>;
   extern __shared__ uint8_t smem_raw[];
   Smem<DQK, FP8> sm;
@@ -842,7 +843,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Sched<VARLEN> sc;
-  sc.tab = &tab;
+  // The unit table comes by value (built on the host) or, when the sequence
+  // offsets live on the device, from global memory (built by a kernel).
+  sc.tab = tab_global ? tab_global : &tab;
   sc.B = a.B;
   sc.Hq = a.Hq;
   sc.Hkv = a.Hkv;
@@ -905,14 +908,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DQK, bool FP8, bool VARLEN, bool LEAN = false>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
-                   const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream) {
+                   const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream,
+                   const typename Sched<VARLEN>::Table* tab_global = nullptr) {
   using C = Cfg<DQK, FP8>;
   auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (n_units == 0) return cudaSuccess;
   const int grid = static_cast<int>(n_units < a.num_sms ? n_units : a.num_sms);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab, tab_global);
   return cudaGetLastError();
 }
 
@@ -953,6 +957,25 @@ cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& t
   if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  return cudaErrorInvalidValue;
+}
+
+// Device-built tables: the unit count is only known on the device, so one
+// CTA per SM; CTAs past the last unit leave at once.
+cudaError_t launch_attn_bf16_varlen_dev(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                        const AttnArgs& a, const SeqTable* tab, cudaStream_t stream) {
+  static const SeqTable unused{};
+  if (a.Dqk == 128) return launch<128, false, true>(tm_q, tm_k, tm_v, a, unused, a.num_sms, stream, tab);
+  if (a.Dqk == 192) return launch<192, false, true>(tm_q, tm_k, tm_v, a, unused, a.num_sms, stream, tab);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fp8_varlen_dev(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                       const AttnArgs& a, const SeqTable* tab, cudaStream_t stream) {
+  static const SeqTable unused{};
+  if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, unused, a.num_sms, stream, tab);
+  if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, unused, a.num_sms, stream, tab);
+  if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, unused, a.num_sms, stream, tab);
   return cudaErrorInvalidValue;
 }
 

@@ -91,4 +91,19 @@ cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& 
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream);
 
+// Offsets on the device: build_seq_tables writes the same tables the host
+// would build into device memory (attn_tab and/or quant_tab, either may be
+// null); offsets that are not a valid partition of `total` tokens into B
+// sequences of at most max_len set kStatusBadSeqlens in *status and leave
+// empty tables, so the kernels that read them do nothing.
+constexpr unsigned int kStatusBadSeqlens = 0x10u;
+cudaError_t launch_build_seq_tables(const int32_t* cu, int B, int total, int max_len, int Hq, SeqTable* attn_tab,
+                                    QuantSeqTable* quant_tab, unsigned int* status, cudaStream_t stream);
+cudaError_t launch_attn_bf16_varlen_dev(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                        const AttnArgs& a, const SeqTable* tab, cudaStream_t stream);
+cudaError_t launch_attn_fp8_varlen_dev(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                       const AttnArgs& a, const SeqTable* tab, cudaStream_t stream);
+cudaError_t launch_quantize_fp8_stream_varlen_dev(const CUtensorMap& tm_x, const QuantArgs& a,
+                                                  const QuantSeqTable* tab, cudaStream_t stream);
+
 }  // namespace zyfa

@@ -171,7 +171,11 @@ template <int D, bool kHadamard, bool VARLEN>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     quantize_fp8_stream_kernel(const __grid_constant__ CUtensorMap tm_x, QuantArgs a,
                                const __grid_constant__ typename std::conditional<VARLEN, QuantSeqTable,
-                                                                                 NoQuantTable>::type tab) {
+                                                                                 NoQuantTable>::type tab_param,
+                               const typename std::conditional<VARLEN, QuantSeqTable, NoQuantTable>::type* tab_global) {
+  // The sequence table comes by value (built on the host) or, when the
+  // offsets live on the device, from global memory (built by a kernel).
+  const auto* tab = tab_global ? tab_global : &tab_param;
   using SC = StreamCfg<D>;
   constexpr int kGroups = D / 64;   // 8-element groups per lane and row
   static_assert(!kHadamard || D == 128, "rotation is defined for head dim 128");
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (a.S + kBlockTokens - 1) / kBlockTokens;
   long long total;
-  if constexpr (VARLEN) total = static_cast<long long>(a.H) * tab.cum_blocks[tab.n_seqs];
+  if constexpr (VARLEN) total = static_cast<long long>(a.H) * tab->cum_blocks[tab->n_seqs];
   else total = static_cast<long long>(a.B) * a.H * (a.blk_hi - a.blk_lo);
   const long long first = blockIdx.x, step = gridDim.x;
 
@@ -192,19 +196,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   auto coords = [&](long long g) {
     QBlock q;
     if constexpr (VARLEN) {
-      int lo = 0, hi = tab.n_seqs - 1;
+      int lo = 0, hi = tab->n_seqs - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<long long>(a.H) * tab.cum_blocks[mid] <= g) lo = mid; else hi = mid - 1;
+        if (static_cast<long long>(a.H) * tab->cum_blocks[mid] <= g) lo = mid; else hi = mid - 1;
       }
-      const int nb = tab.cum_blocks[lo + 1] - tab.cum_blocks[lo];
-      const int r = static_cast<int>(g - static_cast<long long>(a.H) * tab.cum_blocks[lo]);
+      const int nb = tab->cum_blocks[lo + 1] - tab->cum_blocks[lo];
+      const int r = static_cast<int>(g - static_cast<long long>(a.H) * tab->cum_blocks[lo]);
       q.h = r / nb;
       const int blk = r - q.h * nb;
       q.b = 0;
-      q.tok = tab.start[lo] + blk * kBlockTokens;
-      q.valid = min(kBlockTokens, tab.len[lo] - blk * kBlockTokens);
-      q.scale_idx = (static_cast<int64_t>(lo) * a.H + q.h) * tab.max_blocks + blk;
+      q.tok = tab->start[lo] + blk * kBlockTokens;
+      q.valid = min(kBlockTokens, tab->len[lo] - blk * kBlockTokens);
+      q.scale_idx = (static_cast<int64_t>(lo) * a.H + q.h) * tab->max_blocks + blk;
     } else {
       const int range = a.blk_hi - a.blk_lo;
       const int blk = a.blk_lo + static_cast<int>(g % range);
@@ -365,13 +369,13 @@ cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
 
 template <int D, bool H, bool VARLEN, typename Table>
 static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, const Table& tab, long long total,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const Table* tab_global = nullptr) {
   auto kern = quantize_fp8_stream_kernel<D, H, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (total == 0) return cudaSuccess;
   const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
-  kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a, tab);
+  kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a, tab, tab_global);
   return cudaGetLastError();
 }
 
@@ -390,6 +394,18 @@ cudaError_t launch_quantize_fp8_stream_varlen(const CUtensorMap& tm_x, const Qua
   if (a.D == 128 && a.hadamard) return launch_stream<128, true, true>(tm_x, a, tab, total, stream);
   if (a.D == 128) return launch_stream<128, false, true>(tm_x, a, tab, total, stream);
   if (a.D == 192) return launch_stream<192, false, true>(tm_x, a, tab, total, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_fp8_stream_varlen_dev(const CUtensorMap& tm_x, const QuantArgs& a,
+                                                  const QuantSeqTable* tab, cudaStream_t stream) {
+  // The block count is only known on the device: one CTA per SM, each walks
+  // the table's blocks (none when the table is empty).
+  static const QuantSeqTable unused{};
+  const long long total = a.num_sms;
+  if (a.D == 128 && a.hadamard) return launch_stream<128, true, true>(tm_x, a, unused, total, stream, tab);
+  if (a.D == 128) return launch_stream<128, false, true>(tm_x, a, unused, total, stream, tab);
+  if (a.D == 192) return launch_stream<192, false, true>(tm_x, a, unused, total, stream, tab);
   return cudaErrorInvalidValue;
 }
 

@@ -233,11 +233,48 @@ int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, 
                              const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream);
 
 /*
+ * The three packed variable-length calls with cu_seqlens in DEVICE memory
+ * (as a serving stack's batcher leaves them): no host read of the offsets
+ * and no synchronisation. The caller states the packed token count
+ * total_tokens (T, the leading dimension of the packed tensors) and an upper
+ * bound max_seqlen on every sequence's length (it also fixes the scale
+ * layout [B, H, ceil(max_seqlen/128)], so pass the same value to the
+ * quantiser and the attention call). A small kernel builds, in `workspace`,
+ * the same tables the host calls build, so the results are bitwise equal to
+ * theirs. If the offsets on the device are not a partition of T tokens into
+ * B sequences of at most max_seqlen tokens, that call computes nothing and
+ * sets bit 4 of the device status word (zyfa_get_device_status then returns
+ * ZYFA_ERR_INVALID_ARG).
+ *
+ * workspace : device memory of zyfa_varlen_workspace_bytes() bytes, 256-byte
+ *             aligned, owned by the caller; calls on one stream may share it,
+ *             calls that can run concurrently may not.
+ * Other arguments and errors as the host-offset calls.
+ */
+size_t zyfa_varlen_workspace_bytes(void);
+int zyfa_quantize_fp8_varlen_dev(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                                 const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen, int H, int D,
+                                 int hadamard, void* workspace, void* stream);
+int zyfa_attn_fwd_bf16_varlen_dev(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens_dev,
+                                  int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
+                                  float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
+                                  const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
+                                  void* stream);
+int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                                 const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens_dev, int B,
+                                 int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
+                                 float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
+                                 const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
+                                 void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. *word receives the raw bits (0 when every kernel finished normally;
  * bit 0: loader wait timed out, bit 1: MMA wait, bit 2: softmax wait,
- * bit 3: quantiser wait, bit 8: drain after abort incomplete). Returns ZYFA_ERR_TIMEOUT if any bit
- * was set, ZYFA_ERR_CUDA if the synchronisation failed, else ZYFA_OK.
+ * bit 3: quantiser wait, bit 4: invalid device cu_seqlens, bit 8: drain after
+ * abort incomplete). Returns ZYFA_ERR_TIMEOUT if a wait bit was set,
+ * ZYFA_ERR_INVALID_ARG if only bit 4 was, ZYFA_ERR_CUDA if the
+ * synchronisation failed, else ZYFA_OK.
  * `word` may be NULL.
  */
 int zyfa_get_device_status(void* stream, unsigned int* word);

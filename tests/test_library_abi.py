@@ -192,3 +192,29 @@ def test_host_prefill_rejects_bad_arguments_on_host(L):
     assert call(scale=0.0) == 1
     assert call() == 1                        # host buffers are not page-locked
     assert "page-locked" in L.zyfa_last_error_message().decode()
+
+
+def test_device_offset_varlen_rejects_bad_arguments_on_host(L):
+    n = L.zyfa_varlen_workspace_bytes()
+    assert n >= 4 * (2 + 3 * 1024 + 1025) and n % 256 == 0
+    a = L.zyfa_attn_fwd_bf16_varlen_dev
+
+    def call(cu=16, B=2, total=10, max_len=8, ws=256, Hq=2, Hkv=1, D=128):
+        return a(16, 16, 16, 16, cu, B, total, max_len, Hq, Hkv, D, 128, ctypes.c_float(0.1), I2(256, 128),
+                 I2(128, 128), I2(128, 128), I2(256, 128), ws, None)
+
+    assert call(cu=0) == 1                       # no offsets
+    assert call(B=0) == 1
+    assert call(B=1025) == 1
+    assert call(total=-1) == 1
+    assert call(max_len=-1) == 1
+    assert call(max_len=300000) == 2             # longer than the level table
+    assert call(ws=0) == 1                       # no workspace
+    assert call(ws=128) == 1                     # workspace not 256-byte aligned
+    assert call(cu=18) == 1                      # offsets not 4-byte aligned
+    assert call(Hq=3, Hkv=2) == 1
+    assert call(total=0) == 0                    # nothing to compute, nothing enqueued
+    q = L.zyfa_quantize_fp8_varlen_dev
+    assert q(16, 128, 128, 16, 16, 0, 1, 4, 4, 1, 128, 0, 256, None) == 1
+    assert q(16, 128, 128, 16, 16, 16, 1, 4, 4, 1, 64, 0, 256, None) == 2    # D
+    assert q(16, 128, 128, 16, 16, 16, 1, 0, 4, 1, 128, 0, 256, None) == 0   # empty

@@ -90,3 +90,56 @@ def test_sequences_do_not_leak():
     zyfa.device_status()
     assert torch.equal(o1[:200], o2[:200]) and torch.equal(o1[533:], o2[533:])
     assert not torch.equal(o1[200:533], o2[200:533])
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,had", [(4, 2, 128, True), (2, 2, 192, False)])
+@pytest.mark.parametrize("bound", [0, 300])
+def test_device_offsets_reproduce_the_host_tables(Hq, Hkv, D, had, bound):
+    """Offsets left on the device (tables built by a kernel) give the bytes of
+    the host-offset calls; a looser max_seqlen only widens the scale arrays."""
+    q, k, v, cu = _packed(LENS, Hq, Hkv, D, seed=3 * D + bound)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    max_len = max(LENS) + bound
+    o_host = zyfa.attn_fwd_bf16_varlen(qd, kd, vd, cu)
+    o_dev = zyfa.attn_fwd_bf16_varlen(qd, kd, vd, cu_dev, max_seqlen=max_len)
+    f_host, codes_host = zyfa.prefill_fp8_varlen(qd, kd, vd, cu, hadamard=had)
+    f_dev, codes_dev = zyfa.prefill_fp8_varlen(qd, kd, vd, cu_dev, hadamard=had, max_seqlen=max_len)
+    zyfa.device_status()
+    assert torch.equal(o_dev.view(torch.int16), o_host.view(torch.int16))
+    assert torch.equal(f_dev.view(torch.int16), f_host.view(torch.int16))
+    for i in (0, 2, 4):   # codes
+        assert torch.equal(codes_dev[i], codes_host[i])
+    for i in (1, 3, 5):   # scales: the host layout is the leading blocks of the device one
+        nb = codes_host[i].shape[2]
+        for b, n in enumerate(LENS):
+            used = (n + 127) // 128
+            assert torch.equal(codes_dev[i][b, :, :used].view(torch.int32), codes_host[i][b, :, :used].view(torch.int32))
+        assert codes_dev[i].shape[2] >= nb
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "total", "too_long"])
+def test_invalid_device_offsets_compute_nothing_and_are_reported(bad):
+    lens = [100, 300, 50]
+    q, k, v, cu = _packed(lens, 2, 1, 128, seed=21)
+    cu_bad = list(cu)
+    max_len = 300
+    if bad == "decreasing":
+        cu_bad[1], cu_bad[2] = cu_bad[2], cu_bad[1]
+    elif bad == "total":
+        cu_bad[-1] -= 1
+    else:
+        max_len = 299
+    cu_dev = torch.tensor(cu_bad, dtype=torch.int32, device="cuda")
+    zyfa.device_status()
+    out = torch.full((q.shape[0], 2, 128), -7.0, dtype=torch.bfloat16, device="cuda")
+    zyfa.attn_fwd_bf16_varlen(q.cuda(), k.cuda(), v.cuda(), cu_dev, out=out, max_seqlen=max_len)
+    with pytest.raises(zyfa.ZyfaError) as err:
+        zyfa.device_status()
+    assert err.value.code == 1 and "cu_seqlens" in str(err.value)
+    assert bool((out == -7.0).all())
+    codes, scales = zyfa.quantize_fp8_varlen(q.cuda(), cu_dev, max_seqlen=max_len)
+    with pytest.raises(zyfa.ZyfaError):
+        zyfa.device_status()
+    assert bool((scales == 0).all())
+    assert zyfa.device_status() == 0   # the word was cleared
