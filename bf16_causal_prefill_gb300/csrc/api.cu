@@ -92,19 +92,42 @@ int device_info(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// 4-D tiled map over a [B, S, H, D] tensor (dims innermost first: D, H, S, B),
-// box = 128 bytes of D x 1 head x 128 tokens x 1 batch, 128-byte swizzle,
-// out-of-range elements read as zero.
+// 5-D tiled map over a [B, S, H, D] tensor that splits D into 128-byte column
+// blocks and puts tokens before blocks (dims innermost first: 128 bytes of D,
+// S, D / 128 bytes, H, B), so one box = a whole 128-token tile of one head,
+// laid out in shared memory as column block after column block of
+// 128 rows x 128 bytes (the layout the MMA descriptors expect), 128-byte
+// swizzle, out-of-range tokens read as zero.
+// A row that is not a whole number of 128-byte blocks (e4m3 at head dim 192)
+// keeps a 4-D map (D, H, S, B) with a 128-byte box per column block: its last
+// box runs past the row and reads zeros, where a 5-D block would read the
+// next head (or past the tensor).
 int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elt, int D, int H, int S, int B,
              const int64_t strides[3], const char* name) {
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+  if ((D * elt) % 128 != 0) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(strides[2]) * elt,
+                                    static_cast<cuuint64_t>(strides[1]) * elt,
+                                    static_cast<cuuint64_t>(strides[0]) * elt};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), 1u, 128u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, gstrides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+    return ZYFA_OK;
+  }
+  const int inner = 128 / elt;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(D / inner), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(strides[2]) * elt,
-                                  static_cast<cuuint64_t>(strides[1]) * elt,
+  const cuuint64_t gstrides[4] = {static_cast<cuuint64_t>(strides[1]) * elt, 128u,
+                                  static_cast<cuuint64_t>(strides[2]) * elt,
                                   static_cast<cuuint64_t>(strides[0]) * elt};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), 1u, 128u, 1u};
-  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, gstrides, box, estr,
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(inner), 128u, static_cast<cuuint32_t>(D / inner), 1u, 1u};
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = g_encode(map, dt, 5, const_cast<void*>(base), dims, gstrides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);

@@ -99,6 +99,9 @@ struct Cfg {
   static constexpr int kPvSteps = FP8 ? 4 : 8;                  // 128 keys / MMA K
   static constexpr int kPvStepBytes = (FP8 ? 32 : 16) * 128;    // V rows per MMA K step
   static constexpr int kInnerElts = 128 / kElt;                 // TMA box inner extent
+  // Q/K rows of whole 128-byte blocks load as one 5-D request per tile; e4m3
+  // at head dim 192 (1.5 blocks) as one 4-D box per block.
+  static constexpr bool kQkWhole = (kQkRowBytes % 128) == 0;
   // Ring depths (K and V stages of 128 keys).
   static constexpr int kNK = FP8 ? (DQK == 128 ? 4 : 3) : 2;
   static constexpr int kNV = FP8 ? (DQK == 128 ? 6 : 4) : (DQK == 128 ? 3 : 1);
@@ -260,11 +263,12 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 
 // ------------------------------------------------------------------ loader --
 // Two loader warps: one streams Q and K, the other V. A thread's TMA copies
-// are processed one after another (one 16 KB tile takes ~430 cycles however
-// deep the ring is), so a single issuing thread caps the load rate near the
-// tensor pipe's demand; two issuers double it. Each warp runs its loop
-// uniformly (addresses and coordinates stay warp-uniform); one elected lane
-// issues the TMA copies and the expect-tx arrivals.
+// are processed one after another at a roughly fixed cost per request (one
+// 16 KB box takes ~430 cycles however deep the ring is), so each tile, all
+// of its 128-byte column blocks, is one request of a 5-D map, and two
+// issuing warps double the rate. Each warp runs its loop uniformly (addresses
+// and coordinates stay warp-uniform); one elected lane issues the TMA copies
+// and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
 template <int DQK, bool FP8, int STREAM, bool VARLEN>
@@ -273,7 +277,6 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   using C = Cfg<DQK, FP8>;
   constexpr bool kIsK = (STREAM == kStreamQK);
   constexpr int kStages = kIsK ? C::kNK : C::kNV;
-  constexpr int kBlocks = kIsK ? C::kQkBlocks : C::kVBlocks;
   constexpr uint32_t kTileBytes = kIsK ? C::kQkTileBytes : C::kVTileBytes;
   const int n_units = sc.n_units();
   const int group = a.Hq / a.Hkv;
@@ -296,15 +299,15 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
         break;
       if (leader) {
         mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
+        for (int qt = 0; qt < (w.has_b ? 2 : 1); ++qt) {
+          const int row = w.row0 + (2 * w.t + qt) * 128;
+          if constexpr (C::kQkWhole) {
+            tma_load_5d(sm.q_tile(qt), tm_q, sm.q_full(), 0, row, 0, w.hq, w.b);
+          } else {
 #pragma unroll
-        for (int kb = 0; kb < C::kQkBlocks; ++kb)
-          tma_load_4d(sm.q_tile(0) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq,
-                      w.row0 + 2 * w.t * 128, w.b);
-        if (w.has_b) {
-#pragma unroll
-          for (int kb = 0; kb < C::kQkBlocks; ++kb)
-            tma_load_4d(sm.q_tile(1) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq,
-                        w.row0 + (2 * w.t + 1) * 128, w.b);
+            for (int kb = 0; kb < C::kQkBlocks; ++kb)
+              tma_load_4d(sm.q_tile(qt) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, row, w.b);
+          }
         }
       }
       ++qn;
@@ -315,9 +318,13 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
       if (leader) {
         ZTRACE(3, tix, kIsK ? 21 : 23);
         mbar_arrive_expect_tx(full(st), kTileBytes);
+        if constexpr (!kIsK || C::kQkWhole) {
+          tma_load_5d(tile(st), tm_kv, full(st), 0, w.row0 + j * 128, 0, hkv, w.b);
+        } else {
 #pragma unroll
-        for (int kb = 0; kb < kBlocks; ++kb)
-          tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, w.row0 + j * 128, w.b);
+          for (int kb = 0; kb < C::kQkBlocks; ++kb)
+            tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, w.row0 + j * 128, w.b);
+        }
       }
       par = (par & ~(1u << st)) | (ph << st);
       issued |= 1u << st;
