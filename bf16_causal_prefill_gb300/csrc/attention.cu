@@ -442,6 +442,10 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       for (int j = 0; j < w.n_kv; ++j) {
         const bool need_k = (j + 1 < w.n_kv);      // K_{j+1} feeds S_A(j+1) and/or S_B(j+1)
         if (leader) ZTRACE(2, tix, 10);
+#ifdef ZYFA_TRACE
+        if (leader)
+          ZTRACE(2, tix, 40 + (mbar_test(sm.v_full(vs), vph) ? 1 : 0) + (!need_k || mbar_test(sm.k_full(ks), kph) ? 2 : 0));
+#endif
         if (need_k) {
           if (!(ok = warp_wait2(sm.v_full(vs), vph, sm.k_full(ks), kph, abort_flag, a.status, kStatusMmaTimeout,
                                 a.timeout_ns)))
