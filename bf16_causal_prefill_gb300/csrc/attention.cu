@@ -102,6 +102,9 @@ struct Cfg {
   // Q/K rows of whole 128-byte blocks load as one 5-D request per tile; e4m3
   // at head dim 192 (1.5 blocks) as one 4-D box per block.
   static constexpr bool kQkWhole = (kQkRowBytes % 128) == 0;
+  // MMA order per key tile: PV_A, S_A(next), PV_B, S_B(next) (default), or
+  // PV_A, PV_B, S_A(next), S_B(next) where a single V stage fits (bf16, 192).
+  static constexpr bool kLateS = !FP8 && DQK == 192;
   // Ring depths (K and V stages of 128 keys).
   static constexpr int kNK = FP8 ? (DQK == 128 ? 4 : 3) : 2;
   static constexpr int kNV = FP8 ? (DQK == 128 ? 6 : 4) : (DQK == 128 ? 3 : 1);
@@ -454,6 +457,46 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
           ZYFA_WAIT(sm.v_full(vs), vph);
         }
         if (leader) ZTRACE(2, tix, 11);
+        if constexpr (C::kLateS) {
+          // Both PV products of V(j) first, then both next S: V(j) is
+          // released before the two S products run, which hides the load of
+          // V(j+1) behind them when shared memory holds a single V stage.
+          if (j < w.n_a) {
+            ZYFA_WAIT_P(sm.p_full(0), pph0);
+            pph0 ^= 1u;
+            if (leader) {
+              issue_pv<DQK, FP8>(od, tS0, tO0, vs, j > 0);
+              if (j + 1 >= w.n_a) tc_commit(sm.o_full(0));
+            }
+          }
+          if (w.has_b) {
+            ZYFA_WAIT_P(sm.p_full(1), pph1);
+            pph1 ^= 1u;
+            if (leader) {
+              issue_pv<DQK, FP8>(od, tS1, tO1, vs, j > 0);
+              if (j + 1 >= w.n_b) tc_commit(sm.o_full(1));
+            }
+          }
+          if (leader) {
+            tc_commit(sm.v_empty(vs));
+            if (j + 1 < w.n_a) {
+              issue_s<DQK, FP8>(od, tS0, 0, ks);
+              tc_commit(sm.s_full(0));
+              if (!w.has_b && j + 1 == w.n_a - 1) tc_commit(sm.q_empty());
+            }
+            if (w.has_b && j + 1 < w.n_b) {
+              issue_s<DQK, FP8>(od, tS1, 1, ks);
+              tc_commit(sm.s_full(1));
+              if (j + 1 == w.n_b - 1) tc_commit(sm.q_empty());
+            }
+          }
+          if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
+          if (need_k) {
+            if (leader) tc_commit(sm.k_empty(ks));
+            if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+          }
+          continue;
+        }
         if (j < w.n_a) {
           if (leader) ZTRACE(2, tix, 12);
           ZYFA_WAIT_P(sm.p_full(0), pph0);
