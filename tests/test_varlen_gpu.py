@@ -143,3 +143,24 @@ def test_invalid_device_offsets_compute_nothing_and_are_reported(bad):
         zyfa.device_status()
     assert bool((scales == 0).all())
     assert zyfa.device_status() == 0   # the word was cleared
+
+
+def test_device_offsets_at_the_sequence_limit():
+    """1024 sequences (the table's limit), many empty or one token long:
+    the device-built tables give the bytes of the host-built ones."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, 300, size=1024)]
+    lens[17] = 0
+    lens[500] = 1
+    lens[1023] = 777
+    q, k, v, cu = _packed(lens, 2, 1, 128, seed=11)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o_host = zyfa.attn_fwd_bf16_varlen(qd, kd, vd, cu)
+    o_dev = zyfa.attn_fwd_bf16_varlen(qd, kd, vd, cu_dev, max_seqlen=max(lens))
+    c_host, s_host = zyfa.quantize_fp8_varlen(qd, cu)
+    c_dev, s_dev = zyfa.quantize_fp8_varlen(qd, cu_dev, max_seqlen=max(lens))
+    zyfa.device_status()
+    assert torch.equal(o_dev.view(torch.int16), o_host.view(torch.int16))
+    assert torch.equal(c_dev, c_host)
+    assert torch.equal(s_dev.view(torch.int32), s_host.view(torch.int32))
