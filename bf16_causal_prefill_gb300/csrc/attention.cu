@@ -966,8 +966,16 @@ cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUten
                    const typename Sched<VARLEN>::Table* tab_global = nullptr) {
   using C = Cfg<DQK, FP8>;
   auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // The shared-memory opt-in is per function and device: set it once.
+  static bool opted_in[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) opted_in[dev] = true;
+  }
   if (n_units == 0) return cudaSuccess;
   const int grid = static_cast<int>(n_units < a.num_sms ? n_units : a.num_sms);
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab, tab_global);

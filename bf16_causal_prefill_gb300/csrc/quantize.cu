@@ -371,8 +371,16 @@ template <int D, bool H, bool VARLEN, typename Table>
 static cudaError_t launch_stream(const CUtensorMap& tm_x, const QuantArgs& a, const Table& tab, long long total,
                                  cudaStream_t stream, const Table* tab_global = nullptr) {
   auto kern = quantize_fp8_stream_kernel<D, H, VARLEN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<D>::kSmemBytes);
+  // The shared-memory opt-in is per function and device: set it once.
+  static bool opted_in[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) opted_in[dev] = true;
+  }
   if (total == 0) return cudaSuccess;
   const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
   kern<<<grid, kStreamThreads, StreamCfg<D>::kSmemBytes, stream>>>(tm_x, a, tab, tab_global);
