@@ -135,3 +135,18 @@ def test_host_prefill_refuses_pageable_buffers():
     q, k, v = _inputs(1, 256, 2, 1, 128)
     with pytest.raises(ValueError):
         zyfa.prefill_fp8_host(q, k, v)
+
+
+def test_host_prefill_at_the_bench_size_equals_device_path():
+    """The end-to-end configuration the benchmark times (32K GQA, default
+    pieces): same bytes as the device-resident FP8 path, whose outputs the
+    full-size workload tests hold against the oracle."""
+    import workloads
+    w = workloads.get(workloads.BENCH)
+    q, k, v = workloads.make_qkv(w)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    o_dev, _ = zyfa.prefill_fp8(q.cuda(), k.cuda(), v.cuda(), softmax_scale=w.softmax_scale)
+    o_host = zyfa.prefill_fp8_host(hq, hk, hv, softmax_scale=w.softmax_scale)
+    torch.cuda.current_stream().synchronize()
+    zyfa.device_status()
+    assert torch.equal(o_host.view(torch.int16), o_dev.cpu().view(torch.int16))
