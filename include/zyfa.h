@@ -32,6 +32,10 @@
  *   - Every wait inside the kernels is bounded. A kernel that times out
  *     writes a code into a per-device status word and exits cleanly; read it
  *     with zyfa_get_device_status().
+ *   - The device-pointer calls enqueue kernels only (tensor maps and tables
+ *     travel as kernel parameters), so they can be captured into a CUDA
+ *     graph once each kernel configuration has run eagerly on the device
+ *     (the first launch sets its shared-memory opt-in).
  */
 #ifndef ZYFA_H_
 #define ZYFA_H_
