@@ -693,8 +693,13 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
   for (int c = 0; c < 4; ++c) {
     uint32_t r[32];
     tmem_ld32(tO + 32 * c, r);
+    const float2 rr = make_float2(rho, rho);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(u2f(r[e]) * rho);
+    for (int e = 0; e < 16; ++e) {
+      const float2 x = __fmul2_rn(make_float2(u2f(r[2 * e]), u2f(r[2 * e + 1])), rr);
+      r[2 * e] = __float_as_uint(x.x);
+      r[2 * e + 1] = __float_as_uint(x.y);
+    }
     tmem_st32(tO + 32 * c, r);
   }
 }
