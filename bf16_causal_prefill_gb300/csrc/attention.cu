@@ -632,7 +632,7 @@ __device__ __forceinline__ uint32_t lean_e4m3x4_sum(float2 y01, float2 y23, floa
 }
 
 // Probabilities of one 32-column chunk c, p = 2^(s * ca + cb):
-//   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the fp32 p.
+//   BF16: packed bf16 pairs into pk[16c .. 16c+15]; acc sums the rounded p.
 //   FP8:  e4m3 codes, four per word, into pk[8c .. 8c+7]; acc sums the
 //         rounded values.
 template <bool FP8, bool LEAN = false>
@@ -646,8 +646,12 @@ __device__ __forceinline__ void probs_chunk(int c, const uint32_t* s, float ca, 
       const float s0 = u2f(s[2 * i]), s1 = u2f(s[2 * i + 1]);
       const float2 x = __ffma2_rn(make_float2(s0, s1), a2, b2);
       const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      pk[16 * c + i] = pack_bf16x2(p.x, p.y);
-      acc[i & 1] = __fadd2_rn(acc[i & 1], p);
+      const uint32_t pb = pack_bf16x2(p.x, p.y);
+      pk[16 * c + i] = pb;
+      // the row sum adds the rounded values the PV product uses
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+          : "+f"(acc[i & 1].x), "+f"(acc[i & 1].y) : "r"(pb));
     }
   } else {
     // lean P: y = 1024 + 56 + 8x = s * (8 ca) + (8 cb + 1080)
@@ -741,7 +745,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const int n = qt + 1;
     const int hkv = w.hq / group;
     // BF16: m = running max in log2 units (kept while a new maximum stays
-    //       within 2^8 of it), l = sum of the fp32 probabilities.
+    //       within 2^8 of it), l = sum of the bf16-rounded probabilities.
     // FP8:  m = offset o, top = largest log2(p * sv) seen, l = sum of P'/sv.
     float m = 0.f, l = 0.f, top = 0.f;
     float sq = 1.f;

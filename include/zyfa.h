@@ -106,8 +106,9 @@ int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, in
  * Causal attention, BF16 in and out ("ZYFA ..." Introduction; grouped-query
  * heads: query head h reads KV head h / (Hq / Hkv)):
  *   O[b,i,h,:] = sum_{j<=i} softmax_j(softmax_scale * Q[b,i,h].K[b,j,g]) V[b,j,g]
- * Probabilities are rounded to bf16 for the PV product; the row sum uses the
- * unrounded fp32 probabilities; accumulation is fp32; output rounded to bf16.
+ * Probabilities are rounded to bf16 for the PV product and the row sum adds
+ * the same rounded values (the weights of a row sum to one); accumulation is
+ * fp32; output rounded to bf16.
  *
  * q : bf16 [B,S,Hq,Dqk]; k : bf16 [B,S,Hkv,Dqk]; v : bf16 [B,S,Hkv,Dv];
  * o : bf16 [B,S,Hq,Dv], caller-allocated, must not alias q/k/v.
