@@ -688,7 +688,7 @@ __device__ __forceinline__ void probs_row_fp8(uint32_t (&s)[128], float ca, floa
     s[2 * i + 1] = __float_as_uint(ex2_approx(x.y));
   }
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
+  for (int i = 31; i >= 0; --i)
     pk[i] = pack_e4m3x4_sum(u2f(s[4 * i]), u2f(s[4 * i + 1]), u2f(s[4 * i + 2]), u2f(s[4 * i + 3]), acc[i & 1]);
 }
 
