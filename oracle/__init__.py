@@ -21,6 +21,10 @@ What it computes, and the passages it follows:
   mask in float64, the computation the ZYFA kernels perform ("Introduction":
   causal forward attention; "Methodology and Limitations": equal query and
   key lengths), with grouped-query heads.
+* ``attention.causal_attention_prefix`` -- the same definition for queries
+  that continue a cached prefix (query i at position P + i sees keys
+  0 .. P + i); the pages list paged caches as future work ("Methodology and
+  Limitations").
 
 Every function is pinned by ``tests/test_oracle_*.py`` against facts that do
 not come from this package: printed e4m3 codes, torch's float8 cast, SciPy's

@@ -75,6 +75,32 @@ def causal_attention_varlen(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seql
     return out
 
 
+def causal_attention_prefix(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Queries that continue a cached sequence (chunked prefill; the pages
+    name paged caches as future work, "Methodology and Limitations"):
+    q [Lq,Hq,Dqk] holds the last Lq positions of a sequence whose keys and
+    values k [L,Hkv,Dqk], v [L,Hkv,Dv] cover all L >= Lq positions, a prefix
+    of P = L - Lq cached tokens and then the new ones. Query i sits at
+    position P + i and attends to keys 0 .. P + i: the causal definition
+    above with the query index offset by P. Returns O [Lq,Hq,Dv] float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    Lq, Hq, _ = q.shape
+    L, Hkv, _ = k.shape
+    P = L - Lq
+    assert P >= 0, "more queries than positions"
+    allowed = np.arange(L)[None, :] <= (P + np.arange(Lq))[:, None]
+    out = np.empty((Lq, Hq, v.shape[2]), dtype=np.float64)
+    for h in range(Hq):
+        g = kv_head(h, Hq, Hkv)
+        s = np.where(allowed, (q[:, h, :] @ k[:, g, :].T) * scale, -np.inf)
+        s = s - np.max(s, axis=1, keepdims=True)
+        p = np.exp(s)
+        out[:, h, :] = (p / np.sum(p, axis=1, keepdims=True)) @ v[:, g, :]
+    return out
+
+
 def causal_attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                           b: int, h: int, rows: Iterable[int]) -> np.ndarray:
     """Selected output rows of one (batch, query head), one row at a time:
