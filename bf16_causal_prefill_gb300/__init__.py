@@ -98,6 +98,12 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8_varlen.restype = c_int
     L.zyfa_attn_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                            c_float, vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_bf16_paged.restype = c_int
+    L.zyfa_attn_fwd_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int, c_int, c_int,
+                                           c_float, vp, vp, vp, vp, vp]
+    L.zyfa_attn_fwd_fp8_paged.restype = c_int
+    L.zyfa_attn_fwd_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
+                                          c_int, c_int, c_float, vp, vp, vp, vp, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     L.zyfa_set_fp8_probabilities.restype = c_int
@@ -441,6 +447,100 @@ def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seq
     v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream, max_seqlen=max_seqlen)
     o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream, max_seqlen=max_seqlen)
     return o, (q8, qs, k8, ks, v8, vs)
+
+
+def _require_cache(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    _require(t, name, dtype)
+    if t.shape[1] != 128:
+        raise ValueError(f"{name} must be [num_pages, 128, H, D] (pages of 128 tokens)")
+
+
+def _paged_meta(cu_seqlens_q, ctx_lens, block_table: torch.Tensor, device):
+    cu, B, max_len = _cu_host(cu_seqlens_q)
+    if isinstance(ctx_lens, torch.Tensor):
+        ctx_vals = [int(x) for x in ctx_lens.detach().to("cpu", torch.int64).tolist()]
+    else:
+        ctx_vals = [int(x) for x in ctx_lens]
+    if len(ctx_vals) != B:
+        raise ValueError("ctx_lens needs one entry per sequence")
+    ctx = (ctypes.c_int32 * B)(*ctx_vals)
+    if (not block_table.is_cuda or block_table.dtype != torch.int32 or block_table.dim() != 2
+            or block_table.stride(1) != 1 or block_table.shape[0] != B):
+        raise ValueError("block_table must be an int32 CUDA tensor [B, max_pages] with a contiguous last dim")
+    if block_table.device != device:
+        raise ValueError("block_table must be on the same device as the tensors")
+    return cu, ctx, B, max_len
+
+
+def quantize_fp8_cache(cache: torch.Tensor, hadamard: bool = False,
+                       stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-(page, head) e4m3 quantisation of a paged bf16 cache
+    [num_pages, 128, H, D] (each page is one 128-token block). Returns
+    (codes uint8 [num_pages, 128, H, D], scales float32 [num_pages, H])."""
+    _require_cache(cache, "cache", torch.bfloat16)
+    codes, scales = quantize_fp8(cache, hadamard, stream=stream)
+    return codes, scales.view(cache.shape[0], cache.shape[2])
+
+
+def attn_fwd_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cu_seqlens_q, ctx_lens,
+                        block_table: torch.Tensor, softmax_scale: Optional[float] = None,
+                        out: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Packed queries q [T,Hq,Dqk] of B sequences that continue cached ones:
+    sequence i has ctx_lens[i] (a multiple of 128) cached tokens and its new
+    tokens' queries are rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1; its
+    keys/values, new tokens included, are the pages block_table[i] of
+    k_cache/v_cache [num_pages,128,Hkv,D]. Query j attends to positions
+    0 .. ctx_lens[i] + j. Returns o [T,Hq,Dv] bf16."""
+    _require_packed(q, "q", torch.bfloat16)
+    _require_cache(k_cache, "k_cache", torch.bfloat16)
+    _require_cache(v_cache, "v_cache", torch.bfloat16)
+    T, Hq, Dqk = q.shape
+    Hkv, Dv = k_cache.shape[2], v_cache.shape[3]
+    cu, ctx, B, _ = _paged_meta(cu_seqlens_q, ctx_lens, block_table, q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_bf16_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), cu,
+                                          ctx, block_table.data_ptr(), block_table.stride(0), k_cache.shape[0], B,
+                                          Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q), _strides(k_cache),
+                                          _strides(v_cache), _strides2(out), _stream_ptr(q, stream)))
+    return out
+
+
+def attn_fwd_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.Tensor, k_scale: torch.Tensor,
+                       v_cache8: torch.Tensor, v_scale: torch.Tensor, cu_seqlens_q, ctx_lens,
+                       block_table: torch.Tensor, softmax_scale: Optional[float] = None,
+                       out: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """FP8 form of attn_fwd_bf16_paged: q8/q_scale from quantize_fp8_varlen on
+    the packed queries, k/v caches and their [num_pages, Hkv] scales from
+    quantize_fp8_cache. Returns o [T,Hq,Dv] bf16."""
+    _require_packed(q8, "q8", torch.uint8)
+    _require_cache(k_cache8, "k_cache8", torch.uint8)
+    _require_cache(v_cache8, "v_cache8", torch.uint8)
+    T, Hq, Dqk = q8.shape
+    P, Hkv, Dv = k_cache8.shape[0], k_cache8.shape[2], v_cache8.shape[3]
+    cu, ctx, B, max_len = _paged_meta(cu_seqlens_q, ctx_lens, block_table, q8.device)
+    if (not q_scale.is_cuda or q_scale.dtype != torch.float32 or not q_scale.is_contiguous()
+            or tuple(q_scale.shape) != (B, Hq, scale_blocks(max_len))):
+        raise ValueError("q_scale must be a contiguous float32 CUDA tensor [B, Hq, ceil(max_len/128)]")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != P * Hkv:
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor [num_pages, Hkv]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_fwd_fp8_paged(q8.data_ptr(), q_scale.data_ptr(), k_cache8.data_ptr(), k_scale.data_ptr(),
+                                         v_cache8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, ctx,
+                                         block_table.data_ptr(), block_table.stride(0), P, B, Hq, Hkv, Dqk, Dv,
+                                         float(softmax_scale), _strides2(q8), _strides(k_cache8), _strides(v_cache8),
+                                         _strides2(out), _stream_ptr(q8, stream)))
+    return out
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -392,6 +392,38 @@ static int check_dev_seqlens(const int32_t* cu, int B, int total, int max_len, v
   return ZYFA_OK;
 }
 
+// Unit table of a packed batch: non-empty sequences, longest first (ties in
+// batch order); level k holds pair t = n_levels - 1 - k of every sequence
+// with more than t pairs. ctx_blocks (paged K/V) gives each sequence's cached
+// key blocks, else none.
+static void build_seq_table(const int32_t* cu, const int32_t* ctx_blocks, int B, int max_len, int Hq,
+                            zyfa::SeqTable* tab) {
+  std::vector<int> order;
+  for (int i = 0; i < B; ++i)
+    if (cu[i + 1] > cu[i]) order.push_back(i);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int x, int y) { return (cu[x + 1] - cu[x]) > (cu[y + 1] - cu[y]); });
+  tab->n_seqs = static_cast<int>(order.size());
+  for (int i = 0; i < tab->n_seqs; ++i) {
+    tab->start[i] = cu[order[i]];
+    tab->len[i] = cu[order[i] + 1] - cu[order[i]];
+    tab->index[i] = order[i];
+    tab->ctx[i] = ctx_blocks ? ctx_blocks[order[i]] : 0;
+  }
+  auto pairs = [](int len) { return ((len + 127) / 128 + 1) / 2; };
+  tab->n_levels = pairs(max_len);
+  // cnt[t]: sequences with more than t pairs (a prefix of the sorted order)
+  std::vector<int> cnt(tab->n_levels);
+  int with = tab->n_seqs;
+  for (int t = 0; t < tab->n_levels; ++t) {
+    while (with > 0 && pairs(tab->len[with - 1]) <= t) --with;
+    cnt[t] = with;
+  }
+  tab->level_start[0] = 0;
+  for (int kl = 0; kl < tab->n_levels; ++kl)
+    tab->level_start[kl + 1] = tab->level_start[kl] + cnt[tab->n_levels - 1 - kl] * Hq;
+}
+
 static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, const int32_t* cu, int B, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[2], const int64_t ks[2], const int64_t vs[2],
@@ -447,32 +479,8 @@ static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k,
     if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");
     return ZYFA_OK;
   }
-  // Unit table: non-empty sequences, longest first; level k holds pair
-  // t = n_levels - 1 - k of every sequence with more than t pairs.
   static thread_local zyfa::SeqTable tab;
-  std::vector<int> order;
-  for (int i = 0; i < B; ++i)
-    if (cu[i + 1] > cu[i]) order.push_back(i);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int x, int y) { return (cu[x + 1] - cu[x]) > (cu[y + 1] - cu[y]); });
-  tab.n_seqs = static_cast<int>(order.size());
-  for (int i = 0; i < tab.n_seqs; ++i) {
-    tab.start[i] = cu[order[i]];
-    tab.len[i] = cu[order[i] + 1] - cu[order[i]];
-    tab.index[i] = order[i];
-  }
-  auto pairs = [](int len) { return ((len + 127) / 128 + 1) / 2; };
-  tab.n_levels = pairs(max_len);
-  // cnt[t]: sequences with more than t pairs (a prefix of the sorted order)
-  std::vector<int> cnt(tab.n_levels);
-  int with = tab.n_seqs;
-  for (int t = 0; t < tab.n_levels; ++t) {
-    while (with > 0 && pairs(tab.len[with - 1]) <= t) --with;
-    cnt[t] = with;
-  }
-  tab.level_start[0] = 0;
-  for (int kl = 0; kl < tab.n_levels; ++kl)
-    tab.level_start[kl + 1] = tab.level_start[kl] + cnt[tab.n_levels - 1 - kl] * Hq;
+  build_seq_table(cu, nullptr, B, max_len, Hq, &tab);
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_varlen launch" : "attn_fwd_bf16_varlen launch");
@@ -494,6 +502,96 @@ int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k
                              void* stream) {
   return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream);
+}
+
+// Packed queries over a paged K/V cache (chunked prefill, prefix caching).
+static int attn_paged(bool fp8, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
+                      const float* vsc, void* o, const int32_t* cu, const int32_t* ctx_lens,
+                      const int32_t* block_table, int64_t bt_stride, int num_pages, int B, int Hq, int Hkv, int Dqk,
+                      int Dv, float softmax_scale, const int64_t qs[2], const int64_t kcs[3], const int64_t vcs[3],
+                      const int64_t os[2], void* stream) {
+  int T = 0, max_len = 0;
+  if (int r = read_seqlens(cu, B, &T, &max_len)) return r;
+  if (!ctx_lens) return fail(ZYFA_ERR_INVALID_ARG, "ctx_lens is null");
+  if (!block_table || !aligned(block_table, 4)) return fail(ZYFA_ERR_INVALID_ARG, "block_table must be non-null and 4-byte aligned");
+  if (num_pages < 1) return fail(ZYFA_ERR_INVALID_ARG, "num_pages must be >= 1");
+  if (bt_stride < 1) return fail(ZYFA_ERR_INVALID_ARG, "block_table row stride must be >= 1");
+  std::vector<int32_t> ctx_blocks(B);
+  for (int i = 0; i < B; ++i) {
+    const int32_t c = ctx_lens[i];
+    if (c < 0 || c % 128 != 0)
+      return fail(ZYFA_ERR_INVALID_ARG, "ctx_lens[%d] = %d must be a non-negative multiple of 128", i, c);
+    const int64_t blocks = c / 128 + (static_cast<int64_t>(cu[i + 1] - cu[i]) + 127) / 128;
+    if (cu[i + 1] > cu[i] && blocks > bt_stride)
+      return fail(ZYFA_ERR_INVALID_ARG, "sequence %d needs %lld pages, more than the block_table row stride %lld", i,
+                  (long long)blocks, (long long)bt_stride);
+    if (blocks > (1 << 24)) return fail(ZYFA_ERR_UNSUPPORTED, "sequence %d is too long", i);
+    ctx_blocks[i] = c / 128;
+  }
+  if (!qs || !kcs || !vcs || !os) return fail(ZYFA_ERR_INVALID_ARG, "strides pointer is null");
+  if (T == 0) return ZYFA_OK;   // nothing to compute
+  const int64_t q3[3] = {qs[0] * T, qs[0], qs[1]}, o3[3] = {os[0] * T, os[0], os[1]};
+  AttnCommon c{1, T, Hq, Hkv, Dqk, Dv, softmax_scale};
+  const int elt = fp8 ? 1 : 2;
+  // the caches pass the same checks as packed K/V (their strides separately)
+  if (int r = validate_attn(c, q, kc, vc, o, 16 / elt, q3, q3, q3, o3)) return r;
+  if (int r = check_strides(kcs, 16 / elt, "k_cache")) return r;
+  if (int r = check_strides(vcs, 16 / elt, "v_cache")) return r;
+  if (fp8) {
+    if (!qsc || !ksc || !vsc) return fail(ZYFA_ERR_INVALID_ARG, "null scale pointer");
+    if (!aligned(qsc, 4) || !aligned(ksc, 4) || !aligned(vsc, 4))
+      return fail(ZYFA_ERR_INVALID_ARG, "scale pointers must be 4-byte aligned");
+  }
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tq, tk, tv;
+  int r;
+  if ((r = make_map(&tq, q, dt, elt, Dqk, Hq, T, 1, q3, "q")) ||
+      (r = make_map(&tk, kc, dt, elt, Dqk, Hkv, 128, num_pages, kcs, "k_cache")) ||
+      (r = make_map(&tv, vc, dt, elt, Dv, Hkv, 128, num_pages, vcs, "v_cache")))
+    return r;
+  zyfa::AttnArgs a{};
+  a.B = 1; a.S = T; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o; a.o_sb = o3[0]; a.o_ss = o3[1]; a.o_sh = o3[2];
+  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.debug_stall = g_debug_stall;
+  a.num_sms = d->sm_count;
+  a.scale_blocks = (max_len + 127) / 128;
+  a.lean_p = g_lean_p;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.num_pages = num_pages;
+  static thread_local zyfa::SeqTable tab;
+  build_seq_table(cu, ctx_blocks.data(), B, max_len, Hq, &tab);
+  cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
+                      : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_paged launch" : "attn_fwd_bf16_paged launch");
+  return ZYFA_OK;
+}
+
+int zyfa_attn_fwd_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                             const int32_t* cu_seqlens_q, const int32_t* ctx_lens, const int32_t* block_table,
+                             int64_t block_table_stride, int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv,
+                             float softmax_scale, const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                             const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
+  return attn_paged(false, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, cu_seqlens_q, ctx_lens, block_table,
+                    block_table_stride, num_pages, B, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
+                    v_cache_strides, o_strides, stream);
+}
+
+int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
+                            const void* v_cache8, const float* v_scale, void* o, const int32_t* cu_seqlens_q,
+                            const int32_t* ctx_lens, const int32_t* block_table, int64_t block_table_stride,
+                            int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                            const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                            const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
+  return attn_paged(true, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, cu_seqlens_q, ctx_lens, block_table,
+                    block_table_stride, num_pages, B, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
+                    v_cache_strides, o_strides, stream);
 }
 
 static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
@@ -796,9 +894,13 @@ int zyfa_get_device_status(void* stream, unsigned int* word) {
   if ((e = cudaMemcpyToSymbol(zyfa_device_status_word, &zero, sizeof(zero))) != cudaSuccess)
     return fail_cuda(e, "clear status word");
   if (word) *word = w;
-  if (w & ~zyfa::kStatusBadSeqlens) return fail(ZYFA_ERR_TIMEOUT, "device status word 0x%x: a kernel wait timed out", w);
-  if (w) return fail(ZYFA_ERR_INVALID_ARG, "device status word 0x%x: device cu_seqlens were not a valid partition "
-                     "(nothing was computed for that call)", w);
+  if (w & ~(zyfa::kStatusBadSeqlens | zyfa::kStatusBadPage))
+    return fail(ZYFA_ERR_TIMEOUT, "device status word 0x%x: a kernel wait timed out", w);
+  if (w & zyfa::kStatusBadSeqlens)
+    return fail(ZYFA_ERR_INVALID_ARG, "device status word 0x%x: device cu_seqlens were not a valid partition "
+                "(nothing was computed for that call)", w);
+  if (w) return fail(ZYFA_ERR_INVALID_ARG, "device status word 0x%x: a block_table entry was outside the cache "
+                     "(that call's output is meaningless)", w);
   return ZYFA_OK;
 }
 

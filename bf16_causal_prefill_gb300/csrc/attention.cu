@@ -125,6 +125,7 @@ struct Unit {
   int b, hq, t;            // batch coordinate of the maps (0 for packed input), query head, pair
   bool has_b;
   int n_a, n_b, n_kv;
+  int c0;                  // paged K/V: cached key blocks before the first query row (else 0)
   int row0;                // first token of the sequence in the token dimension
   int len;                 // tokens of the sequence
   int sidx;                // sequence index of the scale arrays
@@ -160,6 +161,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
   w.n_a = 2 * w.t + 1;
   w.n_b = 2 * w.t + 2;
   w.n_kv = w.has_b ? w.n_b : w.n_a;
+  w.c0 = 0;
   w.row0 = 0;
   w.sidx = w.b;
   return w;
@@ -195,10 +197,12 @@ struct Sched {
       w.row0 = tab->start[rank];
       w.len = tab->len[rank];
       w.sidx = tab->index[rank];
+      w.c0 = tab->ctx[rank];
       const int nq = (w.len + 127) / 128;
       w.has_b = (2 * w.t + 1) < nq;
-      w.n_a = 2 * w.t + 1;
-      w.n_b = 2 * w.t + 2;
+      // query tile i of the sequence sees key blocks 0 .. c0 + i
+      w.n_a = w.c0 + 2 * w.t + 1;
+      w.n_b = w.c0 + 2 * w.t + 2;
       w.n_kv = w.has_b ? w.n_b : w.n_a;
       return w;
     } else {
@@ -283,6 +287,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   constexpr uint32_t kTileBytes = kIsK ? C::kQkTileBytes : C::kVTileBytes;
   const int n_units = sc.n_units();
   const int group = a.Hq / a.Hkv;
+  const int lane = threadIdx.x & 31;
   volatile int* abort_flag = sm.abort_flag();
   int st = 0;
   uint32_t ph = 0, qn = 0;
@@ -315,18 +320,32 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
       }
       ++qn;
     }
+    int pages = 0;   // paged K/V: block-table entries j & ~31 .. + 31, one per lane
     for (int j = 0; j < w.n_kv; ++j) {
+      // Key block j: tokens row0 + 128 j of batch b, or all 128 tokens of its page.
+      int kv_row = w.row0 + j * 128, kv_b = w.b;
+      if constexpr (VARLEN) {
+        if (a.block_table) {
+          if ((j & 31) == 0) {
+            const int e = j + lane;
+            pages = e < w.n_kv ? __ldg(a.block_table + w.sidx * a.bt_stride + e) : 0;
+          }
+          kv_b = __shfl_sync(0xffffffffu, pages, j & 31);
+          kv_row = 0;
+          if (leader && (kv_b < 0 || kv_b >= a.num_pages)) atomicOr(a.status, kStatusBadPage);
+        }
+      }
       if (leader) ZTRACE(3, tix, kIsK ? 20 : 22);
       if (!(ok = warp_wait(empty(st), ph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns))) break;
       if (leader) {
         ZTRACE(3, tix, kIsK ? 21 : 23);
         mbar_arrive_expect_tx(full(st), kTileBytes);
         if constexpr (!kIsK || C::kQkWhole) {
-          tma_load_5d(tile(st), tm_kv, full(st), 0, w.row0 + j * 128, 0, hkv, w.b);
+          tma_load_5d(tile(st), tm_kv, full(st), 0, kv_row, 0, hkv, kv_b);
         } else {
 #pragma unroll
           for (int kb = 0; kb < C::kQkBlocks; ++kb)
-            tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, w.row0 + j * 128, w.b);
+            tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hkv, kv_row, kv_b);
         }
       }
       par = (par & ~(1u << st)) | (ph << st);
@@ -742,25 +761,37 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
     const int qt = 2 * w.t + wg;
-    const int n = qt + 1;
+    const int n = w.c0 + qt + 1;   // key blocks this query tile sees; the last is on the diagonal
     const int hkv = w.hq / group;
     // BF16: m = running max in log2 units (kept while a new maximum stays
     //       within 2^8 of it), l = sum of the bf16-rounded probabilities.
     // FP8:  m = offset o, top = largest log2(p * sv) seen, l = sum of P'/sv.
     float m = 0.f, l = 0.f, top = 0.f;
     float sq = 1.f;
-    const float* ks_row = nullptr;
-    const float* vs_row = nullptr;
+    int64_t kv_scale_row = 0;
+    int pages = 0;   // paged K/V: block-table entries j & ~31 .. + 31, one per lane
     if constexpr (FP8) {
       sq = __ldg(a.q_scale + (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt);
-      ks_row = a.k_scale + (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
-      vs_row = a.v_scale + (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
+      kv_scale_row = (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
     }
+    (void)pages;
     for (int j = 0; j < n; ++j) {
       float cj = a.scale_log2, lsv = 0.f, inv_sv = 1.f;
       if constexpr (FP8) {
-        const float sk = __ldg(ks_row + j);
-        const float sv = __ldg(vs_row + j);
+        // K/V scales of key block j: per sequence block, or per page.
+        int64_t kv_i = kv_scale_row + j;
+        if constexpr (VARLEN) {
+          if (a.block_table) {
+            if ((j & 31) == 0) {
+              const int e = j + lane;
+              pages = e < n ? __ldg(a.block_table + w.sidx * a.bt_stride + e) : 0;
+            }
+            const int page = min(max(__shfl_sync(0xffffffffu, pages, j & 31), 0), a.num_pages - 1);
+            kv_i = static_cast<int64_t>(page) * a.Hkv + hkv;
+          }
+        }
+        const float sk = __ldg(a.k_scale + kv_i);
+        const float sv = __ldg(a.v_scale + kv_i);
         cj = sq * sk * a.scale_log2;
         lsv = __log2f(sv);
         inv_sv = 1.0f / sv;

@@ -59,6 +59,7 @@ struct SeqTable {
   int start[kMaxVarlenSeqs];           // first token, sorted order
   int len[kMaxVarlenSeqs];             // tokens, sorted order (descending)
   int index[kMaxVarlenSeqs];           // position in the caller's batch
+  int ctx[kMaxVarlenSeqs];             // paged K/V: cached 128-token blocks before the queries (else 0)
   int level_start[kMaxVarlenLevels + 1];   // first unit of each level
 };
 
@@ -77,7 +78,19 @@ struct AttnArgs {
   int scale_blocks;        // fp8: blocks per (sequence, head) row of the scale arrays
   int lean_p;              // fp8, head dim 128: lean P instead of exact P
   int pair_lo, pair_hi;    // equal lengths: only query-tile pairs [pair_lo, pair_hi) (rows 256*lo .. 256*hi)
+  // Paged K/V (packed queries only): key block j of sequence i (caller's
+  // order) is page block_table[i * bt_stride + j] of caches viewed as
+  // [num_pages, 128, Hkv, D]; fp8 K/V scales are [num_pages, Hkv]. Null: K/V
+  // packed like the queries.
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int num_pages;
 };
+
+// A page index outside [0, num_pages): its keys read as zeros (the copy is
+// outside the tensor map) and its fp8 scales are taken from page 0 or the
+// last page; the call's results are meaningless and this bit is set.
+constexpr unsigned int kStatusBadPage = 0x20u;
 
 // tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of
 // 128 bytes x 1 head x 128 tokens x 1 batch.
@@ -86,6 +99,8 @@ cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const AttnArgs& a, cudaStream_t stream);
 // Packed variable-length batch: maps over (D, H, T, 1); `tab` as above.
+// Paged K/V (a.block_table set): tm_k/tm_v over (D, H, 128, num_pages) and
+// tab.ctx gives each sequence's cached blocks.
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream);
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

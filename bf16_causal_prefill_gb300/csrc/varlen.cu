@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       at->start[rank] = start_s[tid];
       at->len[rank] = li;
       at->index[rank] = tid;
+      at->ctx[rank] = 0;
     }
     const int n_levels = pairs_of(longest);
     // Level k holds pair t = n_levels - 1 - k of every sequence with more

@@ -273,12 +273,60 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
                                  void* stream);
 
 /*
+ * Packed queries over a PAGED K/V cache: chunked prefill and prefix caching.
+ * The pages name paged K/V as future work ("ZYFA ...", "Methodology and
+ * Limitations"); this is the cache layout serving stacks use. Sequence i
+ * has ctx_lens[i] tokens already cached and L_i = cu_seqlens_q[i+1] -
+ * cu_seqlens_q[i] new tokens whose queries are rows cu_seqlens_q[i] ..
+ * cu_seqlens_q[i+1]-1 of q [T,Hq,Dqk] (and of o [T,Hq,Dv]); the new tokens'
+ * keys and values must already be in the cache. Query j of sequence i sits
+ * at position ctx_lens[i] + j and attends to cached-sequence positions
+ * 0 .. ctx_lens[i] + j (causal with an offset; ctx_lens[i] = 0 for every i
+ * is the packed varlen call over a paged cache).
+ *
+ * k_cache, v_cache : [num_pages, 128, Hkv, Dqk|Dv], pages of 128 tokens;
+ *              *_cache_strides [3] are the element strides of the page,
+ *              token and head dimensions (last dimension contiguous; the
+ *              alignment rules of the packed calls apply).
+ * block_table : DEVICE int32, row i (block_table + i * block_table_stride)
+ *              lists the pages of sequence i in position order: position p
+ *              is token p % 128 of page row_i[p / 128]. Each row needs
+ *              ctx_lens[i]/128 + ceil(L_i/128) valid entries; the rest are
+ *              not read. An entry outside [0, num_pages) reads zeros, sets
+ *              bit 5 of the device status word and makes that call's output
+ *              meaningless (no fault).
+ * ctx_lens   : HOST int32 [B], each a non-negative multiple of 128 (chunk
+ *              boundaries on page boundaries; ZYFA_ERR_INVALID_ARG otherwise).
+ * cu_seqlens_q : HOST int32 [B+1] as in the packed calls.
+ * Cache slots past a sequence's last position are never attended to, but
+ * the tensor cores still multiply them by a zero probability: keep unused
+ * slots finite (e.g. zero-initialised cache).
+ * FP8: q_scale [B, Hq, ceil(max L_i/128)] from zyfa_quantize_fp8_varlen on
+ *              q; k_scale, v_scale float [num_pages, Hkv], one per page and
+ *              head (zyfa_quantize_fp8 on a cache as B = num_pages, S = 128).
+ * Errors as the packed calls; ZYFA_ERR_INVALID_ARG also for a null
+ * block_table, num_pages < 1, or a row stride too short for a sequence.
+ */
+int zyfa_attn_fwd_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                             const int32_t* cu_seqlens_q, const int32_t* ctx_lens, const int32_t* block_table,
+                             int64_t block_table_stride, int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv,
+                             float softmax_scale, const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                             const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
+int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
+                            const void* v_cache8, const float* v_scale, void* o, const int32_t* cu_seqlens_q,
+                            const int32_t* ctx_lens, const int32_t* block_table, int64_t block_table_stride,
+                            int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                            const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                            const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. *word receives the raw bits (0 when every kernel finished normally;
  * bit 0: loader wait timed out, bit 1: MMA wait, bit 2: softmax wait,
- * bit 3: quantiser wait, bit 4: invalid device cu_seqlens, bit 8: drain after
- * abort incomplete). Returns ZYFA_ERR_TIMEOUT if a wait bit was set,
- * ZYFA_ERR_INVALID_ARG if only bit 4 was, ZYFA_ERR_CUDA if the
+ * bit 3: quantiser wait, bit 4: invalid device cu_seqlens, bit 5: block_table
+ * entry outside the paged cache, bit 8: drain after abort incomplete).
+ * Returns ZYFA_ERR_TIMEOUT if a wait bit was set, ZYFA_ERR_INVALID_ARG if
+ * only bits 4-5 were, ZYFA_ERR_CUDA if the
  * synchronisation failed, else ZYFA_OK.
  * `word` may be NULL.
  */

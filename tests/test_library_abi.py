@@ -218,3 +218,34 @@ def test_device_offset_varlen_rejects_bad_arguments_on_host(L):
     assert q(16, 128, 128, 16, 16, 0, 1, 4, 4, 1, 128, 0, 256, None) == 1
     assert q(16, 128, 128, 16, 16, 16, 1, 4, 4, 1, 64, 0, 256, None) == 2    # D
     assert q(16, 128, 128, 16, 16, 16, 1, 0, 4, 1, 128, 0, 256, None) == 0   # empty
+
+
+def _paged(L, cu, ctx, B, **kw):
+    a = dict(q=16, kc=16, vc=16, o=16, bt=16, bt_stride=4, pages=8, Hq=2, Hkv=1, Dqk=128, Dv=128, scale=0.1,
+             qs=I2(256, 128), kcs=I3(128 * 128, 128, 128), vcs=I3(128 * 128, 128, 128), os_=I2(256, 128))
+    a.update(kw)
+    return L.zyfa_attn_fwd_bf16_paged(a["q"], a["kc"], a["vc"], a["o"], cu, ctx, a["bt"], a["bt_stride"],
+                                      a["pages"], B, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"], ctypes.c_float(a["scale"]),
+                                      a["qs"], a["kcs"], a["vcs"], a["os_"], None)
+
+
+@pytest.mark.parametrize("cu,ctx,B,kw,code", [
+    (_cu(0, 5, 9), None, 2, {}, 1),                           # null ctx_lens
+    (_cu(0, 5, 9), _cu(0, 100), 2, {}, 1),                    # context not on a page boundary
+    (_cu(0, 5, 9), _cu(0, -128), 2, {}, 1),                   # negative context
+    (_cu(0, 5, 9), _cu(0, 512), 2, {}, 1),                    # 4 cached + 1 new page > row stride 4
+    (_cu(0, 5, 9), _cu(0, 384), 2, dict(bt=0), 1),            # null block table
+    (_cu(0, 5, 9), _cu(0, 384), 2, dict(bt=18), 1),           # misaligned block table
+    (_cu(0, 5, 9), _cu(0, 384), 2, dict(pages=0), 1),         # no pages
+    (_cu(0, 5, 9), _cu(0, 384), 2, dict(kcs=I3(128 * 128, 100, 128)), 1),   # cache token stride not 16-byte
+    (_cu(0, 5, 9), _cu(0, 384), 2, dict(Dqk=64, Dv=64), 2),   # head dims
+    (_cu(3, 5, 9), _cu(0, 0), 2, {}, 1),                      # cu_seqlens[0] != 0
+])
+def test_paged_attention_rejects_bad_arguments_on_host(L, cu, ctx, B, kw, code):
+    assert _paged(L, cu, ctx, B, **kw) == code
+    assert L.zyfa_last_error_message()
+
+
+def test_paged_empty_batch_enqueues_nothing(L):
+    # no new tokens: valid, nothing to compute, no device touched
+    assert _paged(L, _cu(0, 0, 0), _cu(128, 0), 2) == 0

@@ -1,0 +1,178 @@
+"""Queries that continue a cached sequence, with K/V in a paged cache
+(chunked prefill, prefix caching), on the GPU against the oracle.
+
+Sequences with and without a cached prefix (empty, one token, ragged tails,
+several tiles) are laid out in 128-token pages in a shuffled order; block
+table entries past what a sequence needs hold an out-of-range page, so a
+read past them would set the device status. BF16 and FP8 outputs are
+compared with the oracle element by element (the cache quantiser's codes and
+scales bit for bit). Two exact consistency checks: no prefix reproduces the
+packed varlen call, and a prefix of r0 tokens reproduces rows r0.. of the
+full-sequence row-range call, byte for byte.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import bf16_causal_prefill_gb300 as zyfa
+from oracle import attention as oattn
+from oracle import fp8 as ofp8
+from parity import assert_bf16_gate, assert_fp8_gate, f32
+
+pytestmark = pytest.mark.gpu
+
+# (cached tokens, new tokens) per sequence
+SEQS = [(0, 300), (256, 129), (640, 1000), (128, 0), (384, 1), (0, 128), (1024, 77)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _sequences(seqs, Hq, Hkv, D, Dv=128, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    for ctx, n in seqs:
+        L = ctx + n
+        out.append((torch.randn(L, Hq, D, generator=g).to(torch.bfloat16),
+                    torch.randn(L, Hkv, D, generator=g).to(torch.bfloat16),
+                    torch.randn(L, Hkv, Dv, generator=g).to(torch.bfloat16)))
+    return out
+
+
+def _paged(seqs, full, extra_pages=3, seed=1):
+    """Packed new queries, shuffled page caches (unused slots zero), block table."""
+    g = torch.Generator().manual_seed(seed)
+    need = [(ctx + n + 127) // 128 if n > 0 else 0 for ctx, n in seqs]
+    P = sum(need) + extra_pages
+    perm = torch.randperm(P, generator=g).tolist()
+    Hkv, D = full[0][1].shape[1], full[0][1].shape[2]
+    Dv = full[0][2].shape[2]
+    kc = torch.zeros(P, 128, Hkv, D, dtype=torch.bfloat16)
+    vc = torch.zeros(P, 128, Hkv, Dv, dtype=torch.bfloat16)
+    width = max(need) + 2
+    bt = torch.full((len(seqs), width), P + 1000, dtype=torch.int32)   # out of range: never read
+    at = 0
+    for i, ((ctx, n), (_, k, v)) in enumerate(zip(seqs, full)):
+        for j in range(need[i]):
+            p = perm[at]
+            at += 1
+            bt[i, j] = p
+            cnt = min(128, ctx + n - 128 * j)
+            kc[p, :cnt] = k[128 * j:128 * j + cnt]
+            vc[p, :cnt] = v[128 * j:128 * j + cnt]
+    q = torch.cat([f[0][ctx:] for (ctx, _), f in zip(seqs, full)])
+    cu = [0]
+    for _, n in seqs:
+        cu.append(cu[-1] + n)
+    return q, kc, vc, bt, cu
+
+
+def _oracle(seqs, qs, ks, vs, scale):
+    outs = [oattn.causal_attention_prefix(q[ctx:], k, v, scale) for (ctx, n), q, k, v in zip(seqs, qs, ks, vs) if n]
+    return np.concatenate(outs)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 2, 128), (2, 2, 192)])
+def test_bf16_paged_matches_oracle(Hq, Hkv, D):
+    full = _sequences(SEQS, Hq, Hkv, D, seed=D)
+    q, kc, vc, bt, cu = _paged(SEQS, full)
+    o = zyfa.attn_fwd_bf16_paged(q.cuda(), kc.cuda(), vc.cuda(), cu, [c for c, _ in SEQS], bt.cuda())
+    zyfa.device_status()
+    ref = _oracle(SEQS, [f32(f[0]) for f in full], [f32(f[1]) for f in full], [f32(f[2]) for f in full],
+                  1 / math.sqrt(D))
+    assert_bf16_gate(f32(o), ref, f"bf16 paged D={D}")
+
+
+def _gather(pages, bt_row, L):
+    return np.concatenate([pages[p] for p in bt_row[:(L + 127) // 128]])[:L]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,had", [(4, 2, 128, False), (4, 2, 128, True), (2, 2, 192, False)])
+def test_fp8_paged_quantiser_and_attention(Hq, Hkv, D, had):
+    full = _sequences(SEQS, Hq, Hkv, D, seed=D + had)
+    q, kc, vc, bt, cu = _paged(SEQS, full)
+    q8, qs = zyfa.quantize_fp8_varlen(q.cuda(), cu, had)
+    kc8, ks = zyfa.quantize_fp8_cache(kc.cuda(), had)
+    vc8, vs = zyfa.quantize_fp8_cache(vc.cuda(), False)
+    o = zyfa.attn_fwd_fp8_paged(q8, qs, kc8, ks, vc8, vs, cu, [c for c, _ in SEQS], bt.cuda())
+    zyfa.device_status()
+    # quantiser: bit-exact against the oracle, pages as 128-token blocks
+    rq, rqs = ofp8.quantize_fp8_varlen(f32(q), cu, had)
+    np.testing.assert_array_equal(q8.cpu().numpy(), rq)
+    deq = []
+    for cache, got_c, got_s, rot in ((kc, kc8, ks, had), (vc, vc8, vs, False)):
+        rc, rs = ofp8.quantize_fp8(f32(cache), rot)
+        np.testing.assert_array_equal(got_c.cpu().numpy(), rc)
+        np.testing.assert_array_equal(got_s.cpu().numpy().view(np.uint32), rs[:, :, 0].view(np.uint32))
+        deq.append(ofp8.dequantize_fp8(rc, rs))
+    qd = ofp8.dequantize_fp8_varlen(rq, rqs, cu)
+    btn = bt.numpy()
+    qs_full, ks_full, vs_full = [], [], []
+    for i, (ctx, n) in enumerate(SEQS):
+        if n == 0:      # no queries: its pages are never read
+            qs_full.append(None), ks_full.append(None), vs_full.append(None)
+            continue
+        qs_full.append(np.concatenate([np.zeros((ctx, Hq, D)), qd[cu[i]:cu[i + 1]]]))
+        ks_full.append(_gather(deq[0], btn[i], ctx + n))
+        vs_full.append(_gather(deq[1], btn[i], ctx + n))
+    ref = _oracle(SEQS, qs_full, ks_full, vs_full, 1 / math.sqrt(D))
+    assert_fp8_gate(f32(o), ref, f"fp8 paged D={D} hadamard={had}")
+
+
+def test_no_prefix_reproduces_the_packed_varlen_call():
+    seqs = [(0, n) for n in (1, 127, 0, 128, 129, 300, 1000, 64, 513)]
+    full = _sequences(seqs, 4, 2, 128, seed=11)
+    q, kc, vc, bt, cu = _paged(seqs, full)
+    k = torch.cat([f[1] for f in full]).cuda()
+    v = torch.cat([f[2] for f in full]).cuda()
+    qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
+    ctx = [0] * len(seqs)
+    assert torch.equal(zyfa.attn_fwd_bf16_paged(qd, kcd, vcd, cu, ctx, btd), zyfa.attn_fwd_bf16_varlen(qd, k, v, cu))
+    q8, qs = zyfa.quantize_fp8_varlen(qd, cu)
+    kc8, ks = zyfa.quantize_fp8_cache(kcd)
+    vc8, vs = zyfa.quantize_fp8_cache(vcd)
+    k8, kss = zyfa.quantize_fp8_varlen(k, cu)
+    v8, vss = zyfa.quantize_fp8_varlen(v, cu)
+    zyfa.device_status()
+    assert torch.equal(zyfa.attn_fwd_fp8_paged(q8, qs, kc8, ks, vc8, vs, cu, ctx, btd),
+                       zyfa.attn_fwd_fp8_varlen(q8, qs, k8, kss, v8, vss, cu))
+    zyfa.device_status()
+
+
+@pytest.mark.parametrize("r0", [256, 512])
+def test_prefix_reproduces_the_row_range_call(r0):
+    S, Hq, Hkv, D = 1000, 4, 2, 128
+    (qf, kf, vf), = _sequences([(0, S)], Hq, Hkv, D, seed=r0)
+    q, kc, vc, bt, cu = _paged([(r0, S - r0)], [(qf, kf, vf)])
+    qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
+    qb, kb, vb = qf.cuda()[None], kf.cuda()[None], vf.cuda()[None]
+    got16 = zyfa.attn_fwd_bf16_paged(qd, kcd, vcd, cu, [r0], btd)
+    ref16 = zyfa.attn_fwd_bf16(qb, kb, vb, rows=(r0, S))[0, r0:]
+    assert torch.equal(got16, ref16)
+    q8, qs = zyfa.quantize_fp8_varlen(qd, cu)
+    kc8, ks = zyfa.quantize_fp8_cache(kcd)
+    vc8, vs = zyfa.quantize_fp8_cache(vcd)
+    fq8, fqs = zyfa.quantize_fp8(qb)
+    fk8, fks = zyfa.quantize_fp8(kb)
+    fv8, fvs = zyfa.quantize_fp8(vb)
+    got8 = zyfa.attn_fwd_fp8_paged(q8, qs, kc8, ks, vc8, vs, cu, [r0], btd)
+    ref8 = zyfa.attn_fwd_fp8(fq8, fqs, fk8, fks, fv8, fvs, rows=(r0, S))[0, r0:]
+    zyfa.device_status()
+    assert torch.equal(got8, ref8)
+
+
+def test_out_of_range_page_sets_the_status_and_reads_zeros():
+    seqs = [(128, 200)]
+    full = _sequences(seqs, 2, 1, 128, seed=5)
+    q, kc, vc, bt, cu = _paged(seqs, full, extra_pages=0)
+    bt[0, 1] = kc.shape[0] + 7          # a page past the cache
+    o = zyfa.attn_fwd_bf16_paged(q.cuda(), kc.cuda(), vc.cuda(), cu, [128], bt.cuda())
+    with pytest.raises(zyfa.ZyfaError):
+        zyfa.device_status()
+    assert zyfa.device_status() == 0     # the status word was cleared
+    assert torch.isfinite(o.float()).all()
