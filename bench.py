@@ -57,6 +57,11 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--chunks", type=int, default=0,
                    help="pieces of the host pipeline along the sequence (0: the library's default)")
+    p.add_argument("--paged", action="store_true",
+                   help="also time the attention kernels over a shuffled paged K/V cache")
+    p.add_argument("--ctx", type=int, default=0,
+                   help="with --paged: cached tokens before the queries (multiple of 128); the last S - ctx "
+                        "tokens are the new chunk")
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -298,6 +303,54 @@ def main_reference(args):
     print(json.dumps(line))
 
 
+def run_paged(args, w, qd, kd, vd, timed, dev):
+    """Kernel-only throughput of the paged calls on the same workload: each
+    batch row's K/V in 128-token pages at shuffled cache positions, the last
+    S - ctx tokens as the new chunk (its queries) after ctx cached ones."""
+    import torch
+    import bf16_causal_prefill_gb300 as zyfa
+    ctx = args.ctx
+    if ctx % 128 or not 0 <= ctx < w.S or w.S % 128:
+        raise SystemExit("--ctx must be a multiple of 128 below S (and S a multiple of 128)")
+    B, S, n = w.B, w.S, w.S // 128
+    Lq = S - ctx
+    perm = torch.randperm(B * n, generator=torch.Generator().manual_seed(0)).to(dev)
+    kc = torch.empty((B * n, 128, w.Hkv, w.Dqk), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty((B * n, 128, w.Hkv, w.Dv), dtype=torch.bfloat16, device=dev)
+    kc[perm] = kd.reshape(B * n, 128, w.Hkv, w.Dqk)
+    vc[perm] = vd.reshape(B * n, 128, w.Hkv, w.Dv)
+    bt = perm.view(B, n).to(torch.int32).contiguous()
+    qn = qd[:, ctx:].reshape(B * Lq, w.Hq, w.Dqk).contiguous()
+    cu = [i * Lq for i in range(B + 1)]
+    ctxs = [ctx] * B
+    had = bool(args.hadamard) and w.Dqk == 128
+    q8, qs = zyfa.quantize_fp8_varlen(qn, cu, had)
+    kc8, ks = zyfa.quantize_fp8_cache(kc, had)
+    vc8, vs = zyfa.quantize_fp8_cache(vc, False)
+    o = torch.empty((B * Lq, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(fp8, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if fp8:
+            zyfa.attn_fwd_fp8_paged(q8, qs, kc8, ks, vc8, vs, cu, ctxs, bt, w.softmax_scale, out=o)
+        else:
+            zyfa.attn_fwd_bf16_paged(qn, kc, vc, cu, ctxs, bt, w.softmax_scale, out=o)
+        if ev is not None:
+            ev[1].record(stream)
+
+    steps = max(3, min(args.steps, 50))
+    _, t8 = timed(lambda ev=None: step(True, ev), steps, 3)
+    _, t16 = timed(lambda ev=None: step(False, ev), steps, 3)
+    # causal FLOPs of the chunk: query i (position ctx + i) sees ctx + i + 1 keys
+    flops = 2.0 * B * w.Hq * (w.Dqk + w.Dv) * (Lq * ctx + Lq * (Lq + 1) / 2)
+    return {"ctx": ctx, "new_tokens": Lq, "page_tokens": 128, "pages": B * n, "steps": steps,
+            "fp8_kernel": flops / (t8 * 1e-3) / 1e12, "bf16_kernel": flops / (t16 * 1e-3) / 1e12, "unit": UNIT,
+            "ms_per_launch": {"fp8": t8, "bf16": t16},
+            "layout": "K/V pages at shuffled cache positions (seeded permutation), block table on the device"}
+
+
 def main():
     args = parse_args()
     if args.cpu_worker:
@@ -408,6 +461,10 @@ def main():
                        "bf16 O -> pinned host, pipelined along the sequence",
                "chunks": args.chunks}
 
+    paged = None
+    if args.paged:
+        paged = run_paged(args, w, qd, kd, vd, timed, dev)
+
     peaks, src = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     fp8_peak_sus = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
@@ -445,6 +502,7 @@ def main():
                               "peak_note": f"bf16 burst (of {src}); sustained-peak frac "
                                            f"{a16 / peaks['bf16_tflops_sustained']:.3f}"}},
         "gpu_launches": 4 * K,
+        **({"paged": paged} if paged is not None else {}),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": None if cpu is None else {
