@@ -487,7 +487,7 @@ def attn_fwd_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
                         out: Optional[torch.Tensor] = None,
                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Packed queries q [T,Hq,Dqk] of B sequences that continue cached ones:
-    sequence i has ctx_lens[i] (a multiple of 128) cached tokens and its new
+    sequence i has ctx_lens[i] cached tokens and its new
     tokens' queries are rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1; its
     keys/values, new tokens included, are the pages block_table[i] of
     k_cache/v_cache [num_pages,128,Hkv,D]. Query j attends to positions

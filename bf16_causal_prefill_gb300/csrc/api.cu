@@ -394,9 +394,9 @@ static int check_dev_seqlens(const int32_t* cu, int B, int total, int max_len, v
 
 // Unit table of a packed batch: non-empty sequences, longest first (ties in
 // batch order); level k holds pair t = n_levels - 1 - k of every sequence
-// with more than t pairs. ctx_blocks (paged K/V) gives each sequence's cached
-// key blocks, else none.
-static void build_seq_table(const int32_t* cu, const int32_t* ctx_blocks, int B, int max_len, int Hq,
+// with more than t pairs. ctx (paged K/V) gives each sequence's cached
+// tokens, else none.
+static void build_seq_table(const int32_t* cu, const int32_t* ctx, int B, int max_len, int Hq,
                             zyfa::SeqTable* tab) {
   std::vector<int> order;
   for (int i = 0; i < B; ++i)
@@ -408,7 +408,7 @@ static void build_seq_table(const int32_t* cu, const int32_t* ctx_blocks, int B,
     tab->start[i] = cu[order[i]];
     tab->len[i] = cu[order[i] + 1] - cu[order[i]];
     tab->index[i] = order[i];
-    tab->ctx[i] = ctx_blocks ? ctx_blocks[order[i]] : 0;
+    tab->ctx[i] = ctx ? ctx[order[i]] : 0;
   }
   auto pairs = [](int len) { return ((len + 127) / 128 + 1) / 2; };
   tab->n_levels = pairs(max_len);
@@ -516,17 +516,14 @@ static int attn_paged(bool fp8, const void* q, const float* qsc, const void* kc,
   if (!block_table || !aligned(block_table, 4)) return fail(ZYFA_ERR_INVALID_ARG, "block_table must be non-null and 4-byte aligned");
   if (num_pages < 1) return fail(ZYFA_ERR_INVALID_ARG, "num_pages must be >= 1");
   if (bt_stride < 1) return fail(ZYFA_ERR_INVALID_ARG, "block_table row stride must be >= 1");
-  std::vector<int32_t> ctx_blocks(B);
   for (int i = 0; i < B; ++i) {
     const int32_t c = ctx_lens[i];
-    if (c < 0 || c % 128 != 0)
-      return fail(ZYFA_ERR_INVALID_ARG, "ctx_lens[%d] = %d must be a non-negative multiple of 128", i, c);
-    const int64_t blocks = c / 128 + (static_cast<int64_t>(cu[i + 1] - cu[i]) + 127) / 128;
+    if (c < 0) return fail(ZYFA_ERR_INVALID_ARG, "ctx_lens[%d] = %d must be non-negative", i, c);
+    const int64_t blocks = (static_cast<int64_t>(c) + (cu[i + 1] - cu[i]) + 127) / 128;
+    if (blocks > (1 << 23)) return fail(ZYFA_ERR_UNSUPPORTED, "sequence %d is too long", i);
     if (cu[i + 1] > cu[i] && blocks > bt_stride)
       return fail(ZYFA_ERR_INVALID_ARG, "sequence %d needs %lld pages, more than the block_table row stride %lld", i,
                   (long long)blocks, (long long)bt_stride);
-    if (blocks > (1 << 24)) return fail(ZYFA_ERR_UNSUPPORTED, "sequence %d is too long", i);
-    ctx_blocks[i] = c / 128;
   }
   if (!qs || !kcs || !vcs || !os) return fail(ZYFA_ERR_INVALID_ARG, "strides pointer is null");
   if (T == 0) return ZYFA_OK;   // nothing to compute
@@ -566,7 +563,7 @@ static int attn_paged(bool fp8, const void* q, const float* qsc, const void* kc,
   a.bt_stride = bt_stride;
   a.num_pages = num_pages;
   static thread_local zyfa::SeqTable tab;
-  build_seq_table(cu, ctx_blocks.data(), B, max_len, Hq, &tab);
+  build_seq_table(cu, ctx_lens, B, max_len, Hq, &tab);
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8_paged launch" : "attn_fwd_bf16_paged launch");

@@ -125,7 +125,7 @@ struct Unit {
   int b, hq, t;            // batch coordinate of the maps (0 for packed input), query head, pair
   bool has_b;
   int n_a, n_b, n_kv;
-  int c0;                  // paged K/V: cached key blocks before the first query row (else 0)
+  int c0, dlt;             // paged K/V: cached tokens before the first query row = 128 c0 + dlt (else 0)
   int row0;                // first token of the sequence in the token dimension
   int len;                 // tokens of the sequence
   int sidx;                // sequence index of the scale arrays
@@ -162,6 +162,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
   w.n_b = 2 * w.t + 2;
   w.n_kv = w.has_b ? w.n_b : w.n_a;
   w.c0 = 0;
+  w.dlt = 0;
   w.row0 = 0;
   w.sidx = w.b;
   return w;
@@ -197,12 +198,18 @@ struct Sched {
       w.row0 = tab->start[rank];
       w.len = tab->len[rank];
       w.sidx = tab->index[rank];
-      w.c0 = tab->ctx[rank];
+      const int ctx = tab->ctx[rank];
+      w.c0 = ctx >> 7;
+      w.dlt = ctx & 127;
       const int nq = (w.len + 127) / 128;
       w.has_b = (2 * w.t + 1) < nq;
-      // query tile i of the sequence sees key blocks 0 .. c0 + i
-      w.n_a = w.c0 + 2 * w.t + 1;
-      w.n_b = w.c0 + 2 * w.t + 2;
+      // Query tile i (positions ctx + 128 i ..) sees key blocks 0 .. c0 + i,
+      // and c0 + i + 1 when the prefix ends inside a block, up to the
+      // sequence's last block.
+      const int nk = (ctx + w.len + 127) >> 7;
+      const int ext = w.dlt ? 1 : 0;
+      w.n_a = min(w.c0 + 2 * w.t + 1 + ext, nk);
+      w.n_b = min(w.c0 + 2 * w.t + 2 + ext, nk);
       w.n_kv = w.has_b ? w.n_b : w.n_a;
       return w;
     } else {
@@ -585,11 +592,11 @@ __device__ __forceinline__ float row_max(const uint32_t (&s)[128]) {
   return max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
-// -inf above the diagonal for the 32 scores of columns col0..col0+31.
-__device__ __forceinline__ void mask_chunk(uint32_t* s, int col0, int r) {
+// -inf for the columns col0..col0+31 above lim (the diagonal: lim = row).
+__device__ __forceinline__ void mask_chunk(uint32_t* s, int col0, int lim) {
 #pragma unroll
   for (int c = 0; c < 32; ++c)
-    if (col0 + c > r) s[c] = 0xff800000u;
+    if (col0 + c > lim) s[c] = 0xff800000u;
 }
 
 // Four floats -> four e4m3 codes (RNE, saturating; v0 in bits 0..7), and
@@ -761,7 +768,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
     const int qt = 2 * w.t + wg;
-    const int n = w.c0 + qt + 1;   // key blocks this query tile sees; the last is on the diagonal
+    const int n = wg ? w.n_b : w.n_a;   // key blocks this query tile sees
     const int hkv = w.hq / group;
     // BF16: m = running max in log2 units (kept while a new maximum stays
     //       within 2^8 of it), l = sum of the bf16-rounded probabilities.
@@ -802,7 +809,19 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       sph ^= 1u;
       tc_fence_after();
       if (tr) ZTRACE(wg, tix, 2);
-      const bool diag = (j == n - 1);
+      // Blocks that reach past a row's position are masked: column c of
+      // block j is key 128 j + c, the row's position is ctx + 128 qt + r, so
+      // columns above lim = 128 (c0 + qt - j) + dlt + r are hidden.
+      bool diag;
+      int lim;
+      if constexpr (VARLEN) {
+        const int jd = j - (w.c0 + qt);
+        diag = jd >= 0;
+        lim = w.dlt + r - 128 * jd;
+      } else {
+        diag = (j == n - 1);
+        lim = r;
+      }
       uint32_t pk[kPk];
       float psum = 0.f;
       const bool first = (j == 0);
@@ -818,7 +837,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         tmem_ld128(tS, s);
         if (diag) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
+          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
         }
         const float bm = row_max(s) * cj + lsv;
         bool moved = false;
@@ -860,7 +879,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         tmem_ld128(tS, s);
         if (diag) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, r);
+          for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
         }
         const float xmax = row_max(s) * cj;
         bool moved = false;

@@ -59,7 +59,7 @@ struct SeqTable {
   int start[kMaxVarlenSeqs];           // first token, sorted order
   int len[kMaxVarlenSeqs];             // tokens, sorted order (descending)
   int index[kMaxVarlenSeqs];           // position in the caller's batch
-  int ctx[kMaxVarlenSeqs];             // paged K/V: cached 128-token blocks before the queries (else 0)
+  int ctx[kMaxVarlenSeqs];             // paged K/V: cached tokens before the queries (else 0)
   int level_start[kMaxVarlenLevels + 1];   // first unit of each level
 };
 
@@ -100,7 +100,7 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
                             const AttnArgs& a, cudaStream_t stream);
 // Packed variable-length batch: maps over (D, H, T, 1); `tab` as above.
 // Paged K/V (a.block_table set): tm_k/tm_v over (D, H, 128, num_pages) and
-// tab.ctx gives each sequence's cached blocks.
+// tab.ctx gives each sequence's cached tokens.
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream);
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

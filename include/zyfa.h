@@ -291,12 +291,12 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
  * block_table : DEVICE int32, row i (block_table + i * block_table_stride)
  *              lists the pages of sequence i in position order: position p
  *              is token p % 128 of page row_i[p / 128]. Each row needs
- *              ctx_lens[i]/128 + ceil(L_i/128) valid entries; the rest are
+ *              ceil((ctx_lens[i] + L_i)/128) valid entries; the rest are
  *              not read. An entry outside [0, num_pages) reads zeros, sets
  *              bit 5 of the device status word and makes that call's output
  *              meaningless (no fault).
- * ctx_lens   : HOST int32 [B], each a non-negative multiple of 128 (chunk
- *              boundaries on page boundaries; ZYFA_ERR_INVALID_ARG otherwise).
+ * ctx_lens   : HOST int32 [B], each >= 0 (any chunk boundary; a chunk of
+ *              one token per sequence is a decode step).
  * cu_seqlens_q : HOST int32 [B+1] as in the packed calls.
  * Cache slots past a sequence's last position are never attended to, but
  * the tensor cores still multiply them by a zero probability: keep unused

@@ -231,7 +231,7 @@ def _paged(L, cu, ctx, B, **kw):
 
 @pytest.mark.parametrize("cu,ctx,B,kw,code", [
     (_cu(0, 5, 9), None, 2, {}, 1),                           # null ctx_lens
-    (_cu(0, 5, 9), _cu(0, 100), 2, {}, 1),                    # context not on a page boundary
+    (_cu(0, 5, 9), _cu(0, 509), 2, {}, 1),                    # 509 cached + 4 new tokens: 5 pages > 4
     (_cu(0, 5, 9), _cu(0, -128), 2, {}, 1),                   # negative context
     (_cu(0, 5, 9), _cu(0, 512), 2, {}, 1),                    # 4 cached + 1 new page > row stride 4
     (_cu(0, 5, 9), _cu(0, 384), 2, dict(bt=0), 1),            # null block table

@@ -1,8 +1,9 @@
 """Queries that continue a cached sequence, with K/V in a paged cache
 (chunked prefill, prefix caching), on the GPU against the oracle.
 
-Sequences with and without a cached prefix (empty, one token, ragged tails,
-several tiles) are laid out in 128-token pages in a shuffled order; block
+Sequences with and without a cached prefix (prefixes on and off page
+boundaries; chunks that are empty, one token, ragged or several tiles) are
+laid out in 128-token pages in a shuffled order; block
 table entries past what a sequence needs hold an out-of-range page, so a
 read past them would set the device status. BF16 and FP8 outputs are
 compared with the oracle element by element (the cache quantiser's codes and
@@ -23,8 +24,10 @@ from parity import assert_bf16_gate, assert_fp8_gate, f32
 
 pytestmark = pytest.mark.gpu
 
-# (cached tokens, new tokens) per sequence
-SEQS = [(0, 300), (256, 129), (640, 1000), (128, 0), (384, 1), (0, 128), (1024, 77)]
+# (cached tokens, new tokens) per sequence: prefixes on and off page
+# boundaries, chunks of one token (a decode step) to several tiles
+SEQS = [(0, 300), (256, 129), (640, 1000), (128, 0), (384, 1), (0, 128), (1024, 77), (5, 300), (300, 129),
+        (127, 1), (1000, 250), (129, 127), (77, 0)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -164,6 +167,38 @@ def test_prefix_reproduces_the_row_range_call(r0):
     ref8 = zyfa.attn_fwd_fp8(fq8, fqs, fk8, fks, fv8, fvs, rows=(r0, S))[0, r0:]
     zyfa.device_status()
     assert torch.equal(got8, ref8)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_steps_match_oracle(fp8):
+    # one new token per sequence after prefixes of any length: a decode step
+    rng = np.random.default_rng(3)
+    seqs = [(int(c), 1) for c in rng.integers(0, 3000, size=16)] + [(0, 1), (127, 1), (128, 1)]
+    Hq, Hkv, D = 8, 2, 128
+    full = _sequences(seqs, Hq, Hkv, D, seed=21 + fp8)
+    q, kc, vc, bt, cu = _paged(seqs, full)
+    ctx = [c for c, _ in seqs]
+    if not fp8:
+        o = zyfa.attn_fwd_bf16_paged(q.cuda(), kc.cuda(), vc.cuda(), cu, ctx, bt.cuda())
+        zyfa.device_status()
+        ref = _oracle(seqs, [f32(f[0]) for f in full], [f32(f[1]) for f in full], [f32(f[2]) for f in full],
+                      1 / math.sqrt(D))
+        assert_bf16_gate(f32(o), ref, "bf16 decode")
+        return
+    q8, qs = zyfa.quantize_fp8_varlen(q.cuda(), cu)
+    kc8, ks = zyfa.quantize_fp8_cache(kc.cuda())
+    vc8, vs = zyfa.quantize_fp8_cache(vc.cuda())
+    o = zyfa.attn_fwd_fp8_paged(q8, qs, kc8, ks, vc8, vs, cu, ctx, bt.cuda())
+    zyfa.device_status()
+    rq, rqs = ofp8.quantize_fp8_varlen(f32(q), cu, False)
+    qd = ofp8.dequantize_fp8_varlen(rq, rqs, cu)
+    kd = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(kc), False))
+    vd = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(vc), False))
+    btn = bt.numpy()
+    ref = np.concatenate([oattn.causal_attention_prefix(qd[i:i + 1], _gather(kd, btn[i], c + 1),
+                                                        _gather(vd, btn[i], c + 1), 1 / math.sqrt(D))
+                          for i, (c, _) in enumerate(seqs)])
+    assert_fp8_gate(f32(o), ref, "fp8 decode")
 
 
 def test_out_of_range_page_sets_the_status_and_reads_zeros():
