@@ -104,6 +104,12 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8_paged.restype = c_int
     L.zyfa_attn_fwd_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
                                           c_int, c_int, c_float, vp, vp, vp, vp, vp]
+    L.zyfa_attn_decode_bf16_paged.restype = c_int
+    L.zyfa_attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int, c_int, c_int,
+                                              c_float, vp, vp, vp, vp, vp]
+    L.zyfa_attn_decode_fp8_paged.restype = c_int
+    L.zyfa_attn_decode_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
+                                             c_int, c_int, c_float, vp, vp, vp, vp, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     L.zyfa_set_fp8_probabilities.restype = c_int
@@ -540,6 +546,88 @@ def attn_fwd_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.
                                          block_table.data_ptr(), block_table.stride(0), P, B, Hq, Hkv, Dqk, Dv,
                                          float(softmax_scale), _strides2(q8), _strides(k_cache8), _strides(v_cache8),
                                          _strides2(out), _stream_ptr(q8, stream)))
+    return out
+
+
+def _decode_meta(seq_lens, block_table: torch.Tensor, N: int, device):
+    if isinstance(seq_lens, torch.Tensor):
+        vals = [int(x) for x in seq_lens.detach().to("cpu", torch.int64).tolist()]
+    else:
+        vals = [int(x) for x in seq_lens]
+    if len(vals) != N:
+        raise ValueError("seq_lens needs one entry per token of q")
+    if (not block_table.is_cuda or block_table.dtype != torch.int32 or block_table.dim() != 2
+            or block_table.stride(1) != 1 or block_table.shape[0] != N):
+        raise ValueError("block_table must be an int32 CUDA tensor [N, max_pages] with a contiguous last dim")
+    if block_table.device != device:
+        raise ValueError("block_table must be on the same device as the tensors")
+    return (ctypes.c_int32 * N)(*vals)
+
+
+def quantize_fp8_decode(q: torch.Tensor, stream: Optional[torch.cuda.Stream] = None,
+                        hadamard: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """e4m3 codes of decode queries q [N,Hq,D] with one scale per token and
+    head. Returns (codes uint8 [N,Hq,D], scales float32 [N,Hq])."""
+    _require_packed(q, "q", torch.bfloat16)
+    codes, scales = quantize_fp8_varlen(q, list(range(q.shape[0] + 1)), hadamard, stream=stream)
+    return codes, scales.view(q.shape[0], q.shape[1])
+
+
+def attn_decode_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens,
+                           block_table: torch.Tensor, softmax_scale: Optional[float] = None,
+                           out: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decode step: q [N,Hq,Dqk] holds each sequence's new token (its K/V
+    already in the cache); sequence i has seq_lens[i] positions, the new one
+    included, in pages block_table[i] of k_cache/v_cache [num_pages,128,Hkv,D].
+    Returns o [N,Hq,Dv] bf16."""
+    _require_packed(q, "q", torch.bfloat16)
+    _require_cache(k_cache, "k_cache", torch.bfloat16)
+    _require_cache(v_cache, "v_cache", torch.bfloat16)
+    N, Hq, Dqk = q.shape
+    Hkv, Dv = k_cache.shape[2], v_cache.shape[3]
+    lens = _decode_meta(seq_lens, block_table, N, q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((N, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_decode_bf16_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                             lens, block_table.data_ptr(), block_table.stride(0), k_cache.shape[0],
+                                             N, Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q),
+                                             _strides(k_cache), _strides(v_cache), _strides2(out),
+                                             _stream_ptr(q, stream)))
+    return out
+
+
+def attn_decode_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.Tensor, k_scale: torch.Tensor,
+                          v_cache8: torch.Tensor, v_scale: torch.Tensor, seq_lens, block_table: torch.Tensor,
+                          softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """FP8 form of attn_decode_bf16_paged: q8/q_scale from quantize_fp8_decode,
+    caches and their [num_pages, Hkv] scales from quantize_fp8_cache."""
+    _require_packed(q8, "q8", torch.uint8)
+    _require_cache(k_cache8, "k_cache8", torch.uint8)
+    _require_cache(v_cache8, "v_cache8", torch.uint8)
+    N, Hq, Dqk = q8.shape
+    P, Hkv, Dv = k_cache8.shape[0], k_cache8.shape[2], v_cache8.shape[3]
+    lens = _decode_meta(seq_lens, block_table, N, q8.device)
+    if not q_scale.is_cuda or q_scale.dtype != torch.float32 or not q_scale.is_contiguous() or q_scale.numel() != N * Hq:
+        raise ValueError("q_scale must be a contiguous float32 CUDA tensor [N, Hq]")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != P * Hkv:
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor [num_pages, Hkv]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    if out is None:
+        out = torch.empty((N, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
+    _require_packed(out, "out", torch.bfloat16)
+    _check(lib().zyfa_attn_decode_fp8_paged(q8.data_ptr(), q_scale.data_ptr(), k_cache8.data_ptr(),
+                                            k_scale.data_ptr(), v_cache8.data_ptr(), v_scale.data_ptr(),
+                                            out.data_ptr(), lens, block_table.data_ptr(), block_table.stride(0), P,
+                                            N, Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q8),
+                                            _strides(k_cache8), _strides(v_cache8), _strides2(out),
+                                            _stream_ptr(q8, stream)))
     return out
 
 

@@ -591,6 +591,112 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
                     v_cache_strides, o_strides, stream);
 }
 
+// Decode step over a paged cache: one query token per sequence.
+static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
+                       const float* vsc, void* o, const int32_t* seq_lens, const int32_t* block_table,
+                       int64_t bt_stride, int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                       const int64_t qs[2], const int64_t kcs[3], const int64_t vcs[3], const int64_t os[2],
+                       void* stream) {
+  if (N < 1 || N > zyfa::kMaxVarlenSeqs)
+    return fail(ZYFA_ERR_INVALID_ARG, "batch %d outside 1..%d", N, zyfa::kMaxVarlenSeqs);
+  if (!seq_lens) return fail(ZYFA_ERR_INVALID_ARG, "seq_lens is null");
+  if (!block_table || !aligned(block_table, 4)) return fail(ZYFA_ERR_INVALID_ARG, "block_table must be non-null and 4-byte aligned");
+  if (num_pages < 1) return fail(ZYFA_ERR_INVALID_ARG, "num_pages must be >= 1");
+  if (bt_stride < 1) return fail(ZYFA_ERR_INVALID_ARG, "block_table row stride must be >= 1");
+  if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || Hq / Hkv > 128)
+    return fail(ZYFA_ERR_INVALID_ARG, "need Hq a multiple of Hkv with at most 128 query heads per KV head");
+  int max_len = 0;
+  for (int i = 0; i < N; ++i) {
+    const int32_t L = seq_lens[i];
+    if (L < 1) return fail(ZYFA_ERR_INVALID_ARG, "seq_lens[%d] = %d must be >= 1 (the new token included)", i, L);
+    if ((static_cast<int64_t>(L) + 127) / 128 > bt_stride)
+      return fail(ZYFA_ERR_INVALID_ARG, "sequence %d needs %lld pages, more than the block_table row stride %lld", i,
+                  (long long)((static_cast<int64_t>(L) + 127) / 128), (long long)bt_stride);
+    max_len = std::max(max_len, L);
+  }
+  if (!qs || !kcs || !vcs || !os) return fail(ZYFA_ERR_INVALID_ARG, "strides pointer is null");
+  if (qs[0] != static_cast<int64_t>(Hq) * qs[1])
+    return fail(ZYFA_ERR_INVALID_ARG, "q must hold each token's heads contiguously (token stride = Hq x head stride)");
+  const int64_t rows = static_cast<int64_t>(N) * Hq;
+  // q as one batch of N*Hq rows (batch, row, "head" strides; the unit batch and head dimensions span it all)
+  const int64_t q3[3] = {qs[1] * rows, qs[1], qs[1] * rows}, o3[3] = {os[0] * N, os[0], os[1]};
+  AttnCommon c{1, N, Hq, Hkv, Dqk, Dv, softmax_scale};
+  const int elt = fp8 ? 1 : 2;
+  if (int r = validate_attn(c, q, kc, vc, o, 16 / elt, q3, q3, q3, o3)) return r;
+  if (int r = check_strides(kcs, 16 / elt, "k_cache")) return r;
+  if (int r = check_strides(vcs, 16 / elt, "v_cache")) return r;
+  if (fp8) {
+    if (!qsc || !ksc || !vsc) return fail(ZYFA_ERR_INVALID_ARG, "null scale pointer");
+    if (!aligned(qsc, 4) || !aligned(ksc, 4) || !aligned(vsc, 4))
+      return fail(ZYFA_ERR_INVALID_ARG, "scale pointers must be 4-byte aligned");
+  }
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return r;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tq, tk, tv;
+  int r;
+  // q as rows of (token, head): the group of a KV head is 128 consecutive rows from its first head
+  if ((r = make_map(&tq, q, dt, elt, Dqk, 1, static_cast<int>(rows), 1, q3, "q")) ||
+      (r = make_map(&tk, kc, dt, elt, Dqk, Hkv, 128, num_pages, kcs, "k_cache")) ||
+      (r = make_map(&tv, vc, dt, elt, Dv, Hkv, 128, num_pages, vcs, "v_cache")))
+    return r;
+  zyfa::AttnArgs a{};
+  a.B = 1; a.S = N; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o; a.o_sb = o3[0]; a.o_ss = o3[1]; a.o_sh = o3[2];
+  a.q_scale = qsc; a.k_scale = ksc; a.v_scale = vsc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns;
+  a.debug_stall = g_debug_stall;
+  a.num_sms = d->sm_count;
+  a.scale_blocks = 1;          // q_scale [N, Hq]: one per token and head
+  a.lean_p = g_lean_p;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.num_pages = num_pages;
+  a.one_token = 1;
+  // Units: sequences by decreasing length (ties in batch order), KV heads adjacent.
+  static thread_local zyfa::SeqTable tab;
+  std::vector<int> order(N);
+  for (int i = 0; i < N; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return seq_lens[x] > seq_lens[y]; });
+  tab.n_seqs = N;
+  tab.n_levels = 0;
+  tab.level_start[0] = 0;
+  for (int i = 0; i < N; ++i) {
+    tab.start[i] = order[i];
+    tab.len[i] = seq_lens[order[i]];
+    tab.index[i] = order[i];
+    tab.ctx[i] = 0;
+  }
+  (void)max_len;
+  cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
+                      : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_decode_fp8 launch" : "attn_decode_bf16 launch");
+  return ZYFA_OK;
+}
+
+int zyfa_attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                const int32_t* seq_lens, const int32_t* block_table, int64_t block_table_stride,
+                                int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                                const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
+  return attn_decode(false, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, seq_lens, block_table,
+                     block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
+                     v_cache_strides, o_strides, stream);
+}
+
+int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
+                               const void* v_cache8, const float* v_scale, void* o, const int32_t* seq_lens,
+                               const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
+                               int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                               const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
+                               const int64_t o_strides[2], void* stream) {
+  return attn_decode(true, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, seq_lens, block_table,
+                     block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
+                     v_cache_strides, o_strides, stream);
+}
+
 static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
                         const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream,
                         const int32_t* cu_dev = nullptr, int total_dev = 0, int max_len_dev = 0,

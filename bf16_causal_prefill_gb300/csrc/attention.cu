@@ -177,12 +177,30 @@ struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
+  bool one_token;          // decode step: one query token per sequence, its heads as tile rows
   __device__ __forceinline__ int n_units() const {
-    if constexpr (VARLEN) return tab->level_start[tab->n_levels];
+    if constexpr (VARLEN) return one_token ? tab->n_seqs * Hkv : tab->level_start[tab->n_levels];
     else return B * Hq * (pair_hi - pair_lo);
   }
   __device__ __forceinline__ Unit decode(int u) const {
     if constexpr (VARLEN) {
+      if (one_token) {
+        // unit = (sequence, KV head); sequences longest first, KV heads adjacent
+        const int rank = u / Hkv;
+        const int h = u - rank * Hkv;
+        Unit w;
+        w.b = 0;
+        w.hq = h * (Hq / Hkv);        // first query head of the group: tile row 0
+        w.t = 0;
+        w.row0 = tab->start[rank];    // the token's row in the packed queries
+        w.len = tab->len[rank];       // keys, the new token's included
+        w.sidx = tab->index[rank];
+        w.c0 = 0;
+        w.dlt = 0;
+        w.has_b = false;
+        w.n_a = w.n_b = w.n_kv = (w.len + 127) >> 7;
+        return w;
+      }
       // level k: the largest with level_start[k] <= u
       int lo = 0, hi = tab->n_levels - 1;
       while (lo < hi) {
@@ -315,13 +333,18 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
       if (leader) {
         mbar_arrive_expect_tx(sm.q_full(), (w.has_b ? 2 : 1) * C::kQkTileBytes);
         for (int qt = 0; qt < (w.has_b ? 2 : 1); ++qt) {
-          const int row = w.row0 + (2 * w.t + qt) * 128;
+          int row = w.row0 + (2 * w.t + qt) * 128, qh = w.hq;
+          if constexpr (VARLEN) {
+            // decode step: the map is over (token, head) rows; the group's
+            // heads are consecutive rows
+            if (sc.one_token) { row = w.row0 * a.Hq + w.hq; qh = 0; }
+          }
           if constexpr (C::kQkWhole) {
-            tma_load_5d(sm.q_tile(qt), tm_q, sm.q_full(), 0, row, 0, w.hq, w.b);
+            tma_load_5d(sm.q_tile(qt), tm_q, sm.q_full(), 0, row, 0, qh, w.b);
           } else {
 #pragma unroll
             for (int kb = 0; kb < C::kQkBlocks; ++kb)
-              tma_load_4d(sm.q_tile(qt) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, w.hq, row, w.b);
+              tma_load_4d(sm.q_tile(qt) + kb * 16384, tm_q, sm.q_full(), kb * C::kInnerElts, qh, row, w.b);
           }
         }
       }
@@ -778,7 +801,12 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     int64_t kv_scale_row = 0;
     int pages = 0;   // paged K/V: block-table entries j & ~31 .. + 31, one per lane
     if constexpr (FP8) {
-      sq = __ldg(a.q_scale + (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt);
+      int64_t qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt;
+      if constexpr (VARLEN) {
+        // decode step: row r is query head hq + r, with its own scale
+        if (sc.one_token) qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq + min(r, group - 1)) * nblk;
+      }
+      sq = __ldg(a.q_scale + qi);
       kv_scale_row = (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
     }
     (void)pages;
@@ -818,6 +846,10 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         const int jd = j - (w.c0 + qt);
         diag = jd >= 0;
         lim = w.dlt + r - 128 * jd;
+        if (sc.one_token) {          // every row is the token at position len - 1
+          diag = (j == n - 1);
+          lim = w.len - 1 - 128 * j;
+        }
       } else {
         diag = (j == n - 1);
         lim = r;
@@ -924,6 +956,13 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     const float inv = 1.f / l;
     const int q_row = qt * 128 + r;
     __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(w.row0 + q_row) * a.o_ss + w.hq * a.o_sh;
+    bool store = q_row < w.len;
+    if constexpr (VARLEN) {
+      if (sc.one_token) {            // row r: query head hq + r of the token
+        orow = out + static_cast<int64_t>(w.row0) * a.o_ss + static_cast<int64_t>(w.hq + r) * a.o_sh;
+        store = r < group;
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
@@ -932,7 +971,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       uint32_t pko[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) pko[e] = pack_bf16x2(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
-      if (q_row < w.len) {
+      if (store) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
         for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pko[4 * v], pko[4 * v + 1], pko[4 * v + 2], pko[4 * v + 3]);
@@ -966,6 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.n_qtiles = (a.S + 127) / 128;
   sc.pair_lo = a.pair_lo;
   sc.pair_hi = a.pair_hi;
+  sc.one_token = a.one_token != 0;
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
@@ -1064,9 +1104,13 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
   return cudaErrorInvalidValue;
 }
 
+long long table_units(const AttnArgs& a, const SeqTable& tab) {
+  return a.one_token ? static_cast<long long>(tab.n_seqs) * a.Hkv : tab.level_start[tab.n_levels];
+}
+
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
-  const long long n = tab.level_start[tab.n_levels];
+  const long long n = table_units(a, tab);
   if (a.Dqk == 128) return launch<128, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;
@@ -1074,7 +1118,7 @@ cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& 
 
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
-  const long long n = tab.level_start[tab.n_levels];
+  const long long n = table_units(a, tab);
   if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);

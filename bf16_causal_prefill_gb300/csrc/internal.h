@@ -85,6 +85,11 @@ struct AttnArgs {
   const int32_t* block_table;
   int64_t bt_stride;
   int num_pages;
+  // Decode step (packed calls only): one query token per sequence; a unit is
+  // (sequence, KV head) and its tile rows are the group's query heads. The
+  // q map is over (token, head) rows, H = 1; tab.len holds each sequence's
+  // key count (the new token included) and tab.start its token's row.
+  int one_token;
 };
 
 // A page index outside [0, num_pages): its keys read as zeros (the copy is

@@ -320,6 +320,36 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
                             const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
 
 /*
+ * Decode step over a paged K/V cache: one new token per sequence (its keys
+ * and values already appended to the cache). Sequence i has seq_lens[i]
+ * positions, the new token's included; its query q[i] (all Hq heads)
+ * attends to positions 0 .. seq_lens[i]-1. Work unit: (sequence, KV head);
+ * the group's Hq/Hkv query heads are the rows of one 128-row tile, so K/V
+ * are read once per KV head. Equal, up to rounding order, to the paged
+ * prefill with ctx_lens[i] = seq_lens[i] - 1 and one new token.
+ *
+ * q, o       : [N, Hq, Dqk|Dv]; q's token stride must be Hq x its head
+ *              stride (each token's heads contiguous).
+ * seq_lens   : HOST int32 [N], each >= 1; 1 <= N <= 1024; Hq/Hkv <= 128.
+ * block_table, k_cache, v_cache, num_pages: as in the paged prefill.
+ * FP8: q_scale float [N, Hq], one per token and head (zyfa_quantize_fp8_varlen
+ *              with one-token sequences writes it); k_scale, v_scale
+ *              [num_pages, Hkv].
+ * Errors as the paged prefill.
+ */
+int zyfa_attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                const int32_t* seq_lens, const int32_t* block_table, int64_t block_table_stride,
+                                int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                                const int64_t q_strides[2], const int64_t k_cache_strides[3],
+                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
+int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
+                               const void* v_cache8, const float* v_scale, void* o, const int32_t* seq_lens,
+                               const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
+                               int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
+                               const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
+                               const int64_t o_strides[2], void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. *word receives the raw bits (0 when every kernel finished normally;
  * bit 0: loader wait timed out, bit 1: MMA wait, bit 2: softmax wait,

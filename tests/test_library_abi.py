@@ -249,3 +249,28 @@ def test_paged_attention_rejects_bad_arguments_on_host(L, cu, ctx, B, kw, code):
 def test_paged_empty_batch_enqueues_nothing(L):
     # no new tokens: valid, nothing to compute, no device touched
     assert _paged(L, _cu(0, 0, 0), _cu(128, 0), 2) == 0
+
+
+def _decode(L, lens, N, **kw):
+    a = dict(q=16, kc=16, vc=16, o=16, bt=16, bt_stride=4, pages=8, Hq=2, Hkv=1, Dqk=128, Dv=128, scale=0.1,
+             qs=I2(256, 128), kcs=I3(128 * 128, 128, 128), vcs=I3(128 * 128, 128, 128), os_=I2(256, 128))
+    a.update(kw)
+    return L.zyfa_attn_decode_bf16_paged(a["q"], a["kc"], a["vc"], a["o"], lens, a["bt"], a["bt_stride"],
+                                         a["pages"], N, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"],
+                                         ctypes.c_float(a["scale"]), a["qs"], a["kcs"], a["vcs"], a["os_"], None)
+
+
+@pytest.mark.parametrize("lens,N,kw,code", [
+    (None, 1, {}, 1),                                  # null seq_lens
+    (_cu(5, 0), 2, {}, 1),                             # a sequence without its new token
+    (_cu(5, 513), 2, {}, 1),                           # 513 positions: 5 pages > row stride 4
+    (_cu(5), 0, {}, 1),                                # no sequence
+    (_cu(5), 1, dict(qs=I2(512, 128)), 1),             # heads of a token not contiguous
+    (_cu(5), 1, dict(Hq=3, Hkv=2), 1),                 # Hq not a multiple of Hkv
+    (_cu(5), 1, dict(Hq=256, Hkv=1, qs=I2(256 * 128, 128)), 1),   # more than 128 heads per KV head
+    (_cu(5), 1, dict(bt=0), 1),                        # null block table
+    (_cu(5), 1, dict(Dqk=64, Dv=64), 2),               # head dims
+])
+def test_decode_rejects_bad_arguments_on_host(L, lens, N, kw, code):
+    assert _decode(L, lens, N, **kw) == code
+    assert L.zyfa_last_error_message()

@@ -211,3 +211,42 @@ def test_out_of_range_page_sets_the_status_and_reads_zeros():
         zyfa.device_status()
     assert zyfa.device_status() == 0     # the status word was cleared
     assert torch.isfinite(o.float()).all()
+
+
+# ----------------------------------------------------------------- decode --
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (32, 1)])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, fp8):
+    """The decode call (query heads of a KV group as tile rows) against the
+    oracle, and byte for byte against the paged prefill with one new token."""
+    rng = np.random.default_rng(Hq + fp8)
+    lens = [int(x) for x in rng.integers(1, 2500, size=13)] + [1, 2, 127, 128, 129, 256]
+    seqs = [(L - 1, 1) for L in lens]
+    D = 128
+    full = _sequences(seqs, Hq, Hkv, D, seed=31 + Hq + fp8)
+    q, kc, vc, bt, cu = _paged(seqs, full)
+    qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
+    ctx = [c for c, _ in seqs]
+    btn = bt.numpy()
+    if fp8:
+        q8, qs = zyfa.quantize_fp8_decode(qd)
+        kc8, ks = zyfa.quantize_fp8_cache(kcd)
+        vc8, vs = zyfa.quantize_fp8_cache(vcd)
+        o = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd)
+        q8p, qsp = zyfa.quantize_fp8_varlen(qd, cu)
+        ref_gpu = zyfa.attn_fwd_fp8_paged(q8p, qsp, kc8, ks, vc8, vs, cu, ctx, btd)
+        zyfa.device_status()
+        assert torch.equal(q8, q8p) and torch.equal(qs.view(-1), qsp.view(-1))
+        rq, rqs = ofp8.quantize_fp8_varlen(f32(q), cu, False)
+        qo = ofp8.dequantize_fp8_varlen(rq, rqs, cu)
+        ko = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(kc), False))
+        vo = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(vc), False))
+    else:
+        o = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd)
+        ref_gpu = zyfa.attn_fwd_bf16_paged(qd, kcd, vcd, cu, ctx, btd)
+        zyfa.device_status()
+        qo, ko, vo = f32(q), f32(kc), f32(vc)
+    ref = np.concatenate([oattn.causal_attention_prefix(qo[i:i + 1], _gather(ko, btn[i], L), _gather(vo, btn[i], L),
+                                                        1 / math.sqrt(D)) for i, L in enumerate(lens)])
+    (assert_fp8_gate if fp8 else assert_bf16_gate)(f32(o), ref, f"decode fp8={fp8} Hq={Hq} Hkv={Hkv}")
+    assert torch.equal(o, ref_gpu)
