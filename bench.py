@@ -62,6 +62,9 @@ def parse_args():
     p.add_argument("--ctx", type=int, default=0,
                    help="with --paged: cached tokens before the queries (multiple of 128); the last S - ctx "
                         "tokens are the new chunk")
+    p.add_argument("--decode", type=int, default=0,
+                   help="also time a decode step: this many sequences of S - 1 cached tokens and one new token, "
+                        "through the paged calls")
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -351,6 +354,54 @@ def run_paged(args, w, qd, kd, vd, timed, dev):
             "layout": "K/V pages at shuffled cache positions (seeded permutation), block table on the device"}
 
 
+def run_decode(args, w, timed, dev):
+    """A decode step through the paged calls: N sequences, each S - 1 cached
+    tokens plus one new token (its query), K/V pages at shuffled positions.
+    Inputs drawn on the device from a seeded generator. Reports the K/V
+    bytes each call must read over its time (the memory roofline of decode)."""
+    import torch
+    import bf16_causal_prefill_gb300 as zyfa
+    N, L = args.decode, w.S
+    n = (L + 127) // 128
+    g = torch.Generator(device=dev).manual_seed(0)
+    kc = torch.randn((N * n, 128, w.Hkv, w.Dqk), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((N * n, 128, w.Hkv, w.Dv), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((N, w.Hq, w.Dqk), generator=g, device=dev).to(torch.bfloat16)
+    perm = torch.randperm(N * n, generator=torch.Generator().manual_seed(1)).to(dev)
+    bt = perm.view(N, n).to(torch.int32).contiguous()
+    cu = list(range(N + 1))
+    ctxs = [L - 1] * N
+    q8, qs = zyfa.quantize_fp8_decode(q)
+    kc8, ks = zyfa.quantize_fp8_cache(kc)
+    vc8, vs = zyfa.quantize_fp8_cache(vc)
+    o = torch.empty((N, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    lens = [L] * N
+    stream = torch.cuda.current_stream(dev)
+
+    def step(fp8, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if fp8:
+            zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, bt, w.softmax_scale, out=o)
+        else:
+            zyfa.attn_decode_bf16_paged(q, kc, vc, lens, bt, w.softmax_scale, out=o)
+        if ev is not None:
+            ev[1].record(stream)
+
+    steps = max(3, min(args.steps, 50))
+    _, t8 = timed(lambda ev=None: step(True, ev), steps, 3)
+    _, t16 = timed(lambda ev=None: step(False, ev), steps, 3)
+    kv8 = N * L * w.Hkv * (w.Dqk + w.Dv)          # bytes of e4m3 K and V the step must read
+    flops = 2.0 * N * w.Hq * (w.Dqk + w.Dv) * L
+    peaks, src = load_peaks()
+    bw = {"fp8": kv8 / (t8 * 1e-3) / 1e9, "bf16": 2 * kv8 / (t16 * 1e-3) / 1e9}
+    return {"seqs": N, "ctx": L - 1, "new_tokens_per_seq": 1, "steps": steps,
+            "ms_per_launch": {"fp8": t8, "bf16": t16}, "kv_read_GBps": bw,
+            "frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in bw.items()}, "hbm_peak_source": src,
+            "tflops": {"fp8": flops / (t8 * 1e-3) / 1e12, "bf16": flops / (t16 * 1e-3) / 1e12},
+            "path": "decode calls: one unit per (sequence, KV head), the group's query heads as tile rows"}
+
+
 def main():
     args = parse_args()
     if args.cpu_worker:
@@ -464,6 +515,9 @@ def main():
     paged = None
     if args.paged:
         paged = run_paged(args, w, qd, kd, vd, timed, dev)
+    decode = None
+    if args.decode > 0:
+        decode = run_decode(args, w, timed, dev)
 
     peaks, src = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
@@ -503,6 +557,7 @@ def main():
                                            f"{a16 / peaks['bf16_tflops_sustained']:.3f}"}},
         "gpu_launches": 4 * K,
         **({"paged": paged} if paged is not None else {}),
+        **({"decode": decode} if decode is not None else {}),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": None if cpu is None else {

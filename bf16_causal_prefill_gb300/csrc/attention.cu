@@ -475,6 +475,54 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
     do {
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
+      if constexpr (VARLEN) {
+        if (sc.one_token) {
+          // Decode step: one query tile; S(j) goes to region j % 2, so S(j+1)
+          // is ready when the softmax finishes tile j. Each PV commits
+          // o_full(1) (a rescale waits for it), the last one o_full(0).
+          const int n = w.n_kv;
+          for (int j = 0; j < 2 && j < n; ++j) {
+            ZYFA_WAIT(sm.k_full(ks), kph);
+            if (leader) {
+              issue_s<DQK, FP8>(od, j ? tS1 : tS0, 0, ks);
+              tc_commit(sm.s_full(j));
+              tc_commit(sm.k_empty(ks));
+              if (j == n - 1) tc_commit(sm.q_empty());
+            }
+            if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+          }
+          if (!ok) break;
+          for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            ZYFA_WAIT(sm.v_full(vs), vph);
+            if (b) {
+              ZYFA_WAIT_P(sm.p_full(1), pph1);
+              pph1 ^= 1u;
+            } else {
+              ZYFA_WAIT_P(sm.p_full(0), pph0);
+              pph0 ^= 1u;
+            }
+            if (leader) {
+              issue_pv<DQK, FP8>(od, b ? tS1 : tS0, tO0, vs, j > 0);
+              tc_commit(sm.o_full(1));
+              if (j == n - 1) tc_commit(sm.o_full(0));
+              tc_commit(sm.v_empty(vs));
+            }
+            if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
+            if (j + 2 < n) {
+              ZYFA_WAIT(sm.k_full(ks), kph);
+              if (leader) {
+                issue_s<DQK, FP8>(od, b ? tS1 : tS0, 0, ks);
+                tc_commit(sm.s_full(b));
+                tc_commit(sm.k_empty(ks));
+                if (j + 2 == n - 1) tc_commit(sm.q_empty());
+              }
+              if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+            }
+          }
+          break;
+        }
+      }
       ZYFA_WAIT(sm.k_full(ks), kph);
       if (leader) ZTRACE(2, tix, 26);
       if (leader) {
@@ -767,6 +815,23 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
 // with no measurable change in the output error.
 constexpr float kWinLo = -4.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
 
+// Decode step: S of the next tile can complete before the PV product of the
+// previous one has run, so a tile that rescales O first waits for that
+// product (the k-th PV commit on o_full(1), k counted from 0 per CTA).
+// Elsewhere O is final when S completes (the PV was issued before it).
+template <int DQK, bool FP8, bool VARLEN>
+__device__ __forceinline__ bool wait_pv_done(const Smem<DQK, FP8>& sm, const Sched<VARLEN>& sc, uint32_t k,
+                                             volatile int* abort_flag, const AttnArgs& a) {
+  if constexpr (VARLEN) {
+    if (sc.one_token) {
+      const bool ok = mbar_wait(sm.o_full(1), k & 1u, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return false; }
+      tc_fence_after();
+    }
+  }
+  return true;
+}
+
 template <int DQK, bool FP8, bool VARLEN, bool LEAN>
 __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
                              int warp, int lane) {
@@ -780,7 +845,8 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   const uint32_t tS = tmem + wg * 128 + lane_off;
   const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
   constexpr int kPk = FP8 ? 32 : 64;
-  uint32_t sph = 0, oph = 0;
+  uint32_t sph = 0, oph = 0;   // sph: parity bit of s_full(0) and s_full(1)
+  uint32_t pvn = 0;            // decode step: PV products committed so far on o_full(1)
   uint32_t tix = 0;
   const bool tr = lane == 0 && (warp & 3) == 0;
   (void)tix;
@@ -810,31 +876,67 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       kv_scale_row = (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
     }
     (void)pages;
+    // Index of the K/V scales of key block jj (called with jj = 0, 1, ...):
+    // per sequence block, or per page (block table read 32 entries at a
+    // time, one per lane).
+    auto kv_index = [&](int jj) -> int64_t {
+      int64_t kv_i = kv_scale_row + jj;
+      if constexpr (VARLEN) {
+        if (a.block_table) {
+          if ((jj & 31) == 0) {
+            const int e = jj + lane;
+            pages = e < n ? __ldg(a.block_table + w.sidx * a.bt_stride + e) : 0;
+          }
+          const int page = min(max(__shfl_sync(0xffffffffu, pages, jj & 31), 0), a.num_pages - 1);
+          kv_i = static_cast<int64_t>(page) * a.Hkv + hkv;
+        }
+      }
+      return kv_i;
+    };
+    // Packed and paged inputs load the next block's scales one tile ahead
+    // (in a decode step S is often ready before these loads would return).
+    float sk_next = 0.f, sv_next = 0.f;
+    if constexpr (FP8 && VARLEN) {
+      const int64_t i0 = kv_index(0);
+      sk_next = __ldg(a.k_scale + i0);
+      sv_next = __ldg(a.v_scale + i0);
+    }
     for (int j = 0; j < n; ++j) {
       float cj = a.scale_log2, lsv = 0.f, inv_sv = 1.f;
       if constexpr (FP8) {
-        // K/V scales of key block j: per sequence block, or per page.
-        int64_t kv_i = kv_scale_row + j;
+        float sk, sv;
         if constexpr (VARLEN) {
-          if (a.block_table) {
-            if ((j & 31) == 0) {
-              const int e = j + lane;
-              pages = e < n ? __ldg(a.block_table + w.sidx * a.bt_stride + e) : 0;
-            }
-            const int page = min(max(__shfl_sync(0xffffffffu, pages, j & 31), 0), a.num_pages - 1);
-            kv_i = static_cast<int64_t>(page) * a.Hkv + hkv;
+          sk = sk_next;
+          sv = sv_next;
+          if (j + 1 < n) {
+            const int64_t i1 = kv_index(j + 1);
+            sk_next = __ldg(a.k_scale + i1);
+            sv_next = __ldg(a.v_scale + i1);
           }
+        } else {
+          const int64_t kv_i = kv_index(j);
+          sk = __ldg(a.k_scale + kv_i);
+          sv = __ldg(a.v_scale + kv_i);
         }
-        const float sk = __ldg(a.k_scale + kv_i);
-        const float sv = __ldg(a.v_scale + kv_i);
         cj = sq * sk * a.scale_log2;
         lsv = __log2f(sv);
         inv_sv = 1.0f / sv;
       }
+      // S (and P over it) of this tile: the warpgroup's own region, or in a
+      // decode step the two regions in turn (tile j + 1 is computed while
+      // tile j is in the softmax).
+      int bj = wg;
+      uint32_t tSj = tS;
+      if constexpr (VARLEN) {
+        if (sc.one_token) {
+          bj = j & 1;
+          tSj = tmem + bj * 128 + lane_off;
+        }
+      }
       if (tr) ZTRACE(wg, tix, 1);
-      bool ok = mbar_wait(sm.s_full(wg), sph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
+      bool ok = mbar_wait(sm.s_full(bj), (sph >> bj) & 1u, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return; }
-      sph ^= 1u;
+      sph ^= 1u << bj;
       tc_fence_after();
       if (tr) ZTRACE(wg, tix, 2);
       // Blocks that reach past a row's position are masked: column c of
@@ -866,7 +968,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         // faster than computing the exponentials speculatively and redoing
         // them, for a few percent on rows that rarely move it.
         uint32_t s[128];
-        tmem_ld128(tS, s);
+        tmem_ld128(tSj, s);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
@@ -900,7 +1002,10 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         psum = t.x + t.y;
         // O is final for the previous tiles (their PV completed before this
         // S); rescaling it after the exponentials keeps S out of registers.
-        if (moved) rescale_o_row(tO, rho);
+        if (moved) {
+          if (!wait_pv_done(sm, sc, pvn + j - 1, abort_flag, a)) return;
+          rescale_o_row(tO, rho);
+        }
       } else {
         // The whole row of S in one load and its maximum first. The first
         // tile sets the running maximum; later tiles keep it stale while
@@ -908,7 +1013,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         // exponentials (O is rescaled after them). No tile computes its
         // exponentials twice.
         uint32_t s[128];
-        tmem_ld128(tS, s);
+        tmem_ld128(tSj, s);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
@@ -933,20 +1038,24 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         for (int c = 0; c < 4; ++c) probs_chunk<false>(c, &s[32 * c], cj, -m, pk, acc);
         const float2 t = __fadd2_rn(acc[0], acc[1]);
         psum = t.x + t.y;
-        if (moved) rescale_o_row(tO, rho);
+        if (moved) {
+          if (!wait_pv_done(sm, sc, pvn + j - 1, abort_flag, a)) return;
+          rescale_o_row(tO, rho);
+        }
       }
       if (tr) ZTRACE(wg, tix, 3);
       if constexpr (FP8) l = fmaf(psum, inv_sv, l);
       else l += psum;
 #pragma unroll
-      for (int c = 0; c < kPk / 32; ++c) tmem_st32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * c]));
+      for (int c = 0; c < kPk / 32; ++c) tmem_st32(tSj + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * c]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.p_full(wg));
+      if (lane == 0) mbar_arrive(sm.p_full(bj));
       if (tr) ZTRACE(wg, tix, 4);
     }
 
+    pvn += n;
     // epilogue: O / l, BF16, global store
     if (tr) ZTRACE(wg, tix, 5);
     bool ok = mbar_wait(sm.o_full(wg), oph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
