@@ -179,28 +179,33 @@ struct Sched {
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
   bool one_token;          // decode step: one query token per sequence, its heads as tile rows
   __device__ __forceinline__ int n_units() const {
-    if constexpr (VARLEN) return one_token ? tab->n_seqs * Hkv : tab->level_start[tab->n_levels];
+    if constexpr (VARLEN) return one_token ? (tab->n_seqs * Hkv + 1) / 2 : tab->level_start[tab->n_levels];
     else return B * Hq * (pair_hi - pair_lo);
   }
+  // Decode step: task i = (sequence of rank i / Hkv, KV head i % Hkv), the
+  // sequences longest first and KV heads adjacent; unit u runs tasks 2u (as
+  // tile A) and 2u + 1 (as tile B), each with its own K/V stream.
+  __device__ __forceinline__ Unit decode_task(int i, bool second) const {
+    const int rank = i / Hkv;
+    const int h = i - rank * Hkv;
+    Unit w;
+    w.b = 0;
+    w.hq = h * (Hq / Hkv);        // first query head of the group: tile row 0
+    w.t = 0;
+    w.row0 = tab->start[rank];    // the token's row in the packed queries
+    w.len = tab->len[rank];       // keys, the new token's included
+    w.sidx = tab->index[rank];
+    w.c0 = 0;
+    w.dlt = 0;
+    w.has_b = second;
+    w.n_a = w.n_b = w.n_kv = (w.len + 127) >> 7;
+    return w;
+  }
+  // Tile B of a decode unit (call only when decode(u).has_b).
+  __device__ __forceinline__ Unit decode_b(int u) const { return decode_task(2 * u + 1, true); }
   __device__ __forceinline__ Unit decode(int u) const {
     if constexpr (VARLEN) {
-      if (one_token) {
-        // unit = (sequence, KV head); sequences longest first, KV heads adjacent
-        const int rank = u / Hkv;
-        const int h = u - rank * Hkv;
-        Unit w;
-        w.b = 0;
-        w.hq = h * (Hq / Hkv);        // first query head of the group: tile row 0
-        w.t = 0;
-        w.row0 = tab->start[rank];    // the token's row in the packed queries
-        w.len = tab->len[rank];       // keys, the new token's included
-        w.sidx = tab->index[rank];
-        w.c0 = 0;
-        w.dlt = 0;
-        w.has_b = false;
-        w.n_a = w.n_b = w.n_kv = (w.len + 127) >> 7;
-        return w;
-      }
+      if (one_token) return decode_task(2 * u, 2 * u + 1 < tab->n_seqs * Hkv);
       // level k: the largest with level_start[k] <= u
       int lo = 0, hi = tab->n_levels - 1;
       while (lo < hi) {
@@ -335,9 +340,13 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
         for (int qt = 0; qt < (w.has_b ? 2 : 1); ++qt) {
           int row = w.row0 + (2 * w.t + qt) * 128, qh = w.hq;
           if constexpr (VARLEN) {
-            // decode step: the map is over (token, head) rows; the group's
-            // heads are consecutive rows
-            if (sc.one_token) { row = w.row0 * a.Hq + w.hq; qh = 0; }
+            // decode step: the map is over (token, head) rows; a group's
+            // heads are consecutive rows; tile B holds the second task
+            if (sc.one_token) {
+              const Unit x = qt ? sc.decode_b(u) : w;
+              row = x.row0 * a.Hq + x.hq;
+              qh = 0;
+            }
           }
           if constexpr (C::kQkWhole) {
             tma_load_5d(sm.q_tile(qt), tm_q, sm.q_full(), 0, row, 0, qh, w.b);
@@ -349,6 +358,45 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
         }
       }
       ++qn;
+    }
+    if constexpr (VARLEN) {
+      if (sc.one_token) {
+        // Decode step: the two tasks' key blocks alternate in the ring
+        // (A0, B0, A1, B1, ...; a finished task drops out), the order in
+        // which the MMA warp consumes them.
+        const Unit wb = w.has_b ? sc.decode_b(u) : w;
+        const int na = w.n_kv, nb = w.has_b ? wb.n_kv : 0;
+        int pg[2] = {0, 0};
+        for (int j = 0; j < max(na, nb) && ok; ++j) {
+          for (int x = 0; x < 2; ++x) {
+            const Unit& wx = x ? wb : w;
+            if (j >= (x ? nb : na)) continue;
+            if ((j & 31) == 0) {
+              const int e = j + lane;
+              pg[x] = e < wx.n_kv ? __ldg(a.block_table + wx.sidx * a.bt_stride + e) : 0;
+            }
+            const int page = __shfl_sync(0xffffffffu, pg[x], j & 31);
+            if (leader && (page < 0 || page >= a.num_pages)) atomicOr(a.status, kStatusBadPage);
+            if (!(ok = warp_wait(empty(st), ph ^ 1u, abort_flag, a.status, kStatusLoaderTimeout, a.timeout_ns)))
+              break;
+            if (leader) {
+              mbar_arrive_expect_tx(full(st), kTileBytes);
+              const int hx = wx.hq / group;
+              if constexpr (!kIsK || C::kQkWhole) {
+                tma_load_5d(tile(st), tm_kv, full(st), 0, 0, 0, hx, page);
+              } else {
+#pragma unroll
+                for (int kb = 0; kb < C::kQkBlocks; ++kb)
+                  tma_load_4d(tile(st) + kb * 16384, tm_kv, full(st), kb * C::kInnerElts, hx, 0, page);
+              }
+            }
+            par = (par & ~(1u << st)) | (ph << st);
+            issued |= 1u << st;
+            if (++st == kStages) { st = 0; ph ^= 1u; }
+          }
+        }
+        continue;
+      }
     }
     int pages = 0;   // paged K/V: block-table entries j & ~31 .. + 31, one per lane
     for (int j = 0; j < w.n_kv; ++j) {
@@ -477,47 +525,56 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       ++qn;
       if constexpr (VARLEN) {
         if (sc.one_token) {
-          // Decode step: one query tile; S(j) goes to region j % 2, so S(j+1)
-          // is ready when the softmax finishes tile j. Each PV commits
-          // o_full(1) (a rescale waits for it), the last one o_full(0).
-          const int n = w.n_kv;
-          for (int j = 0; j < 2 && j < n; ++j) {
+          // Decode step: tasks A and B of the unit are independent chains
+          // (own K/V blocks, interleaved in the rings), ping-ponged like two
+          // query tiles: S_A(0), S_B(0), then per block PV_X(j), S_X(j+1).
+          const int na = w.n_kv, nb = w.has_b ? sc.decode_b(u).n_kv : 0;
+          const int n_s = na + nb;        // S products of the unit; Q is free after the last
+          int s_done = 0;
+          for (int x = 0; x < 2; ++x) {
+            if ((x ? nb : na) == 0) continue;
             ZYFA_WAIT(sm.k_full(ks), kph);
             if (leader) {
-              issue_s<DQK, FP8>(od, j ? tS1 : tS0, 0, ks);
-              tc_commit(sm.s_full(j));
+              issue_s<DQK, FP8>(od, x ? tS1 : tS0, x, ks);
+              tc_commit(sm.s_full(x));
               tc_commit(sm.k_empty(ks));
-              if (j == n - 1) tc_commit(sm.q_empty());
+              if (++s_done == n_s) tc_commit(sm.q_empty());
+            } else {
+              ++s_done;
             }
             if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
           }
           if (!ok) break;
-          for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
-            ZYFA_WAIT(sm.v_full(vs), vph);
-            if (b) {
-              ZYFA_WAIT_P(sm.p_full(1), pph1);
-              pph1 ^= 1u;
-            } else {
-              ZYFA_WAIT_P(sm.p_full(0), pph0);
-              pph0 ^= 1u;
-            }
-            if (leader) {
-              issue_pv<DQK, FP8>(od, b ? tS1 : tS0, tO0, vs, j > 0);
-              tc_commit(sm.o_full(1));
-              if (j == n - 1) tc_commit(sm.o_full(0));
-              tc_commit(sm.v_empty(vs));
-            }
-            if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
-            if (j + 2 < n) {
-              ZYFA_WAIT(sm.k_full(ks), kph);
-              if (leader) {
-                issue_s<DQK, FP8>(od, b ? tS1 : tS0, 0, ks);
-                tc_commit(sm.s_full(b));
-                tc_commit(sm.k_empty(ks));
-                if (j + 2 == n - 1) tc_commit(sm.q_empty());
+          for (int j = 0; j < max(na, nb) && ok; ++j) {
+            for (int x = 0; x < 2; ++x) {
+              const int nx = x ? nb : na;
+              if (j >= nx) continue;
+              ZYFA_WAIT(sm.v_full(vs), vph);
+              if (x) {
+                ZYFA_WAIT_P(sm.p_full(1), pph1);
+                pph1 ^= 1u;
+              } else {
+                ZYFA_WAIT_P(sm.p_full(0), pph0);
+                pph0 ^= 1u;
               }
-              if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+              if (leader) {
+                issue_pv<DQK, FP8>(od, x ? tS1 : tS0, x ? tO1 : tO0, vs, j > 0);
+                if (j + 1 == nx) tc_commit(sm.o_full(x));
+                tc_commit(sm.v_empty(vs));
+              }
+              if (++vs == C::kNV) { vs = 0; vph ^= 1u; }
+              if (j + 1 < nx) {
+                ZYFA_WAIT(sm.k_full(ks), kph);
+                if (leader) {
+                  issue_s<DQK, FP8>(od, x ? tS1 : tS0, x, ks);
+                  tc_commit(sm.s_full(x));
+                  tc_commit(sm.k_empty(ks));
+                  if (++s_done == n_s) tc_commit(sm.q_empty());
+                } else {
+                  ++s_done;
+                }
+                if (++ks == C::kNK) { ks = 0; kph ^= 1u; }
+              }
             }
           }
           break;
@@ -815,23 +872,6 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
 // with no measurable change in the output error.
 constexpr float kWinLo = -4.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
 
-// Decode step: S of the next tile can complete before the PV product of the
-// previous one has run, so a tile that rescales O first waits for that
-// product (the k-th PV commit on o_full(1), k counted from 0 per CTA).
-// Elsewhere O is final when S completes (the PV was issued before it).
-template <int DQK, bool FP8, bool VARLEN>
-__device__ __forceinline__ bool wait_pv_done(const Smem<DQK, FP8>& sm, const Sched<VARLEN>& sc, uint32_t k,
-                                             volatile int* abort_flag, const AttnArgs& a) {
-  if constexpr (VARLEN) {
-    if (sc.one_token) {
-      const bool ok = mbar_wait(sm.o_full(1), k & 1u, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
-      if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return false; }
-      tc_fence_after();
-    }
-  }
-  return true;
-}
-
 template <int DQK, bool FP8, bool VARLEN, bool LEAN>
 __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
                              int warp, int lane) {
@@ -845,8 +885,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   const uint32_t tS = tmem + wg * 128 + lane_off;
   const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
   constexpr int kPk = FP8 ? 32 : 64;
-  uint32_t sph = 0, oph = 0;   // sph: parity bit of s_full(0) and s_full(1)
-  uint32_t pvn = 0;            // decode step: PV products committed so far on o_full(1)
+  uint32_t sph = 0, oph = 0;
   uint32_t tix = 0;
   const bool tr = lane == 0 && (warp & 3) == 0;
   (void)tix;
@@ -854,8 +893,11 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o);
 
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Unit w = sc.decode(u);
+    Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
+    if constexpr (VARLEN) {
+      if (sc.one_token && wg == 1) w = sc.decode_b(u);   // decode step: tile B runs the unit's second task
+    }
     const int qt = 2 * w.t + wg;
     const int n = wg ? w.n_b : w.n_a;   // key blocks this query tile sees
     const int hkv = w.hq / group;
@@ -922,21 +964,10 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         lsv = __log2f(sv);
         inv_sv = 1.0f / sv;
       }
-      // S (and P over it) of this tile: the warpgroup's own region, or in a
-      // decode step the two regions in turn (tile j + 1 is computed while
-      // tile j is in the softmax).
-      int bj = wg;
-      uint32_t tSj = tS;
-      if constexpr (VARLEN) {
-        if (sc.one_token) {
-          bj = j & 1;
-          tSj = tmem + bj * 128 + lane_off;
-        }
-      }
       if (tr) ZTRACE(wg, tix, 1);
-      bool ok = mbar_wait(sm.s_full(bj), (sph >> bj) & 1u, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
+      bool ok = mbar_wait(sm.s_full(wg), sph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return; }
-      sph ^= 1u << bj;
+      sph ^= 1u;
       tc_fence_after();
       if (tr) ZTRACE(wg, tix, 2);
       // Blocks that reach past a row's position are masked: column c of
@@ -968,7 +999,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         // faster than computing the exponentials speculatively and redoing
         // them, for a few percent on rows that rarely move it.
         uint32_t s[128];
-        tmem_ld128(tSj, s);
+        tmem_ld128(tS, s);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
@@ -1002,10 +1033,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         psum = t.x + t.y;
         // O is final for the previous tiles (their PV completed before this
         // S); rescaling it after the exponentials keeps S out of registers.
-        if (moved) {
-          if (!wait_pv_done(sm, sc, pvn + j - 1, abort_flag, a)) return;
-          rescale_o_row(tO, rho);
-        }
+        if (moved) rescale_o_row(tO, rho);
       } else {
         // The whole row of S in one load and its maximum first. The first
         // tile sets the running maximum; later tiles keep it stale while
@@ -1013,7 +1041,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         // exponentials (O is rescaled after them). No tile computes its
         // exponentials twice.
         uint32_t s[128];
-        tmem_ld128(tSj, s);
+        tmem_ld128(tS, s);
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) mask_chunk(&s[32 * c], 32 * c, lim);
@@ -1038,24 +1066,20 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         for (int c = 0; c < 4; ++c) probs_chunk<false>(c, &s[32 * c], cj, -m, pk, acc);
         const float2 t = __fadd2_rn(acc[0], acc[1]);
         psum = t.x + t.y;
-        if (moved) {
-          if (!wait_pv_done(sm, sc, pvn + j - 1, abort_flag, a)) return;
-          rescale_o_row(tO, rho);
-        }
+        if (moved) rescale_o_row(tO, rho);
       }
       if (tr) ZTRACE(wg, tix, 3);
       if constexpr (FP8) l = fmaf(psum, inv_sv, l);
       else l += psum;
 #pragma unroll
-      for (int c = 0; c < kPk / 32; ++c) tmem_st32(tSj + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * c]));
+      for (int c = 0; c < kPk / 32; ++c) tmem_st32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * c]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.p_full(bj));
+      if (lane == 0) mbar_arrive(sm.p_full(wg));
       if (tr) ZTRACE(wg, tix, 4);
     }
 
-    pvn += n;
     // epilogue: O / l, BF16, global store
     if (tr) ZTRACE(wg, tix, 5);
     bool ok = mbar_wait(sm.o_full(wg), oph, abort_flag, a.status, kStatusSoftmaxTimeout, a.timeout_ns);
