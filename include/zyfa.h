@@ -323,10 +323,11 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  * Decode step over a paged K/V cache: one new token per sequence (its keys
  * and values already appended to the cache). Sequence i has seq_lens[i]
  * positions, the new token's included; its query q[i] (all Hq heads)
- * attends to positions 0 .. seq_lens[i]-1. Work unit: (sequence, KV head);
+ * attends to positions 0 .. seq_lens[i]-1. A task is (sequence, KV head):
  * the group's Hq/Hkv query heads are the rows of one 128-row tile, so K/V
- * are read once per KV head. Equal, up to rounding order, to the paged
- * prefill with ctx_lens[i] = seq_lens[i] - 1 and one new token.
+ * are read once per KV head; each CTA runs two tasks as its two query tiles.
+ * The results are the bytes of the paged prefill with ctx_lens[i] =
+ * seq_lens[i] - 1 and one new token.
  *
  * q, o       : [N, Hq, Dqk|Dv]; q's token stride must be Hq x its head
  *              stride (each token's heads contiguous).
