@@ -104,12 +104,14 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8_paged.restype = c_int
     L.zyfa_attn_fwd_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
                                           c_int, c_int, c_float, vp, vp, vp, vp, vp]
+    L.zyfa_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.zyfa_decode_workspace_bytes.argtypes = [c_int, c_int, c_int]
     L.zyfa_attn_decode_bf16_paged.restype = c_int
     L.zyfa_attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int, c_int, c_int,
-                                              c_float, vp, vp, vp, vp, vp]
+                                              c_float, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.zyfa_attn_decode_fp8_paged.restype = c_int
     L.zyfa_attn_decode_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
-                                             c_int, c_int, c_float, vp, vp, vp, vp, vp]
+                                             c_int, c_int, c_float, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     L.zyfa_set_fp8_probabilities.restype = c_int
@@ -564,6 +566,21 @@ def _decode_meta(seq_lens, block_table: torch.Tensor, N: int, device):
     return (ctypes.c_int32 * N)(*vals)
 
 
+def _decode_workspace(N: int, Hq: int, Hkv: int, device, split, stream):
+    """(pointer, bytes, tensor) of the split-key-range workspace: split=True
+    allocates one, a uint8 CUDA tensor is used as given, False/None gives none."""
+    if split is False or split is None:
+        return None, 0, None
+    if isinstance(split, torch.Tensor):
+        if not split.is_cuda or split.dtype != torch.uint8:
+            raise ValueError("workspace must be a uint8 CUDA tensor")
+        return split.data_ptr(), split.numel(), split
+    ws = torch.empty(lib().zyfa_decode_workspace_bytes(N, Hq, Hkv), dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)
+    return ws.data_ptr(), ws.numel(), ws
+
+
 def quantize_fp8_decode(q: torch.Tensor, stream: Optional[torch.cuda.Stream] = None,
                         hadamard: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """e4m3 codes of decode queries q [N,Hq,D] with one scale per token and
@@ -576,11 +593,13 @@ def quantize_fp8_decode(q: torch.Tensor, stream: Optional[torch.cuda.Stream] = N
 def attn_decode_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens,
                            block_table: torch.Tensor, softmax_scale: Optional[float] = None,
                            out: Optional[torch.Tensor] = None,
-                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                           stream: Optional[torch.cuda.Stream] = None, split=True) -> torch.Tensor:
     """One decode step: q [N,Hq,Dqk] holds each sequence's new token (its K/V
     already in the cache); sequence i has seq_lens[i] positions, the new one
     included, in pages block_table[i] of k_cache/v_cache [num_pages,128,Hkv,D].
-    Returns o [N,Hq,Dv] bf16."""
+    split: True (allocate a workspace so long key ranges may be split across
+    SMs), a uint8 CUDA workspace tensor, or False (no split: the bytes of the
+    paged prefill with one new token). Returns o [N,Hq,Dv] bf16."""
     _require_packed(q, "q", torch.bfloat16)
     _require_cache(k_cache, "k_cache", torch.bfloat16)
     _require_cache(v_cache, "v_cache", torch.bfloat16)
@@ -592,10 +611,11 @@ def attn_decode_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if out is None:
         out = torch.empty((N, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     _require_packed(out, "out", torch.bfloat16)
+    ws_ptr, ws_bytes, _ws = _decode_workspace(N, Hq, Hkv, q.device, split, stream)
     _check(lib().zyfa_attn_decode_bf16_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
                                              lens, block_table.data_ptr(), block_table.stride(0), k_cache.shape[0],
                                              N, Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q),
-                                             _strides(k_cache), _strides(v_cache), _strides2(out),
+                                             _strides(k_cache), _strides(v_cache), _strides2(out), ws_ptr, ws_bytes,
                                              _stream_ptr(q, stream)))
     return out
 
@@ -603,7 +623,7 @@ def attn_decode_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
 def attn_decode_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.Tensor, k_scale: torch.Tensor,
                           v_cache8: torch.Tensor, v_scale: torch.Tensor, seq_lens, block_table: torch.Tensor,
                           softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                          stream: Optional[torch.cuda.Stream] = None, split=True) -> torch.Tensor:
     """FP8 form of attn_decode_bf16_paged: q8/q_scale from quantize_fp8_decode,
     caches and their [num_pages, Hkv] scales from quantize_fp8_cache."""
     _require_packed(q8, "q8", torch.uint8)
@@ -622,11 +642,12 @@ def attn_decode_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: tor
     if out is None:
         out = torch.empty((N, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
     _require_packed(out, "out", torch.bfloat16)
+    ws_ptr, ws_bytes, _ws = _decode_workspace(N, Hq, Hkv, q8.device, split, stream)
     _check(lib().zyfa_attn_decode_fp8_paged(q8.data_ptr(), q_scale.data_ptr(), k_cache8.data_ptr(),
                                             k_scale.data_ptr(), v_cache8.data_ptr(), v_scale.data_ptr(),
                                             out.data_ptr(), lens, block_table.data_ptr(), block_table.stride(0), P,
                                             N, Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q8),
-                                            _strides(k_cache8), _strides(v_cache8), _strides2(out),
+                                            _strides(k_cache8), _strides(v_cache8), _strides2(out), ws_ptr, ws_bytes,
                                             _stream_ptr(q8, stream)))
     return out
 

@@ -591,12 +591,31 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
                     v_cache_strides, o_strides, stream);
 }
 
+// Decode step: key ranges are split only while there are fewer than
+// kSplitTasksPerSm (sequence, KV head) tasks per SM, into splits of at least
+// kMinSplitTiles / 2 key blocks; the workspace holds the partial rows of up
+// to kSplitTasksPerSm tasks per SM on kMaxSmsForWorkspace SMs, plus one per
+// sequence.
+constexpr int kSplitTasksPerSm = 4;
+constexpr int kMinSplitTiles = 8;
+constexpr int kMaxSmsForWorkspace = 256;
+
+static size_t decode_partial_rows_bound(int N, int Hkv) {
+  return static_cast<size_t>(kSplitTasksPerSm) * kMaxSmsForWorkspace / std::max(Hkv, 1) + 1 + std::max(N, 0);
+}
+
+static size_t decode_ws_bytes(int N, int Hq, int Hkv) {
+  // per partial row and head: 128 fp32 of O and (m, l)
+  const size_t rows = decode_partial_rows_bound(N, Hkv) * static_cast<size_t>(std::max(Hq, 0));
+  return ((rows * 128 * 4 + 255) & ~size_t(255)) + rows * 2 * 4;
+}
+
 // Decode step over a paged cache: one query token per sequence.
 static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
                        const float* vsc, void* o, const int32_t* seq_lens, const int32_t* block_table,
                        int64_t bt_stride, int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                        const int64_t qs[2], const int64_t kcs[3], const int64_t vcs[3], const int64_t os[2],
-                       void* stream) {
+                       void* workspace, size_t workspace_bytes, void* stream) {
   if (N < 1 || N > zyfa::kMaxVarlenSeqs)
     return fail(ZYFA_ERR_INVALID_ARG, "batch %d outside 1..%d", N, zyfa::kMaxVarlenSeqs);
   if (!seq_lens) return fail(ZYFA_ERR_INVALID_ARG, "seq_lens is null");
@@ -670,20 +689,86 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
     tab.ctx[i] = 0;
   }
   (void)max_len;
+  // Split key ranges when that shortens the schedule: CTA c runs units c,
+  // c + num_sms, ... (a unit = two tasks of one sequence and split), so the
+  // step takes about the largest sum of unit lengths over the CTAs. Each
+  // candidate split length (key blocks) is scored that way, plus a start-up
+  // cost per unit; splits of a sequence are nearly equal.
+  static thread_local zyfa::CombineTable ct;
+  int chunk = 0;
+  if (workspace && static_cast<int64_t>(N) * Hkv < static_cast<int64_t>(kSplitTasksPerSm) * d->sm_count) {
+    const int G = d->sm_count;
+    auto makespan = [&](int c) {   // c = 0: no split
+      std::vector<int64_t> load(G, 0);
+      int64_t unit = 0;
+      for (int k = 0; k < N; ++k) {
+        const int n = (tab.len[k] + 127) / 128;
+        const int S = c ? (n + c - 1) / c : 1;
+        for (int sp = 0; sp < S; ++sp) {
+          const int len = n / S + (sp < n % S ? 1 : 0);
+          for (int h = 0; h < Hkv; h += 2) load[unit++ % G] += len + 2;
+        }
+      }
+      return *std::max_element(load.begin(), load.end());
+    };
+    int64_t best = makespan(0);
+    for (int c = kMinSplitTiles; c < 1 << 16; c *= 2) {
+      bool any = false;
+      size_t rows = 0;
+      for (int k = 0; k < N; ++k) {
+        const int n = (tab.len[k] + 127) / 128;
+        any = any || n > c;
+        rows += (n + c - 1) / c;
+      }
+      if (!any) break;
+      if (rows > decode_partial_rows_bound(N, Hkv)) continue;   // more partial rows than the workspace holds
+      const int64_t m = makespan(c);
+      if (m < best) { best = m; chunk = c; }
+    }
+  }
+  if (chunk) {
+    if (!aligned(workspace, 256)) return fail(ZYFA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < decode_ws_bytes(N, Hq, Hkv))
+      return fail(ZYFA_ERR_INVALID_ARG, "workspace of %zu bytes is below zyfa_decode_workspace_bytes = %zu",
+                  workspace_bytes, decode_ws_bytes(N, Hq, Hkv));
+    int rows = 0;
+    for (int k = 0; k < N; ++k) {
+      const int splits = ((tab.len[k] + 127) / 128 + chunk - 1) / chunk;   // each at least chunk/2 blocks
+      tab.level_start[k] = rows * Hkv;
+      tab.ctx[k] = rows;
+      ct.base[tab.index[k]] = rows;
+      ct.count[tab.index[k]] = splits;
+      rows += splits;
+    }
+    tab.level_start[N] = rows * Hkv;
+    if (static_cast<size_t>(rows) > decode_partial_rows_bound(N, Hkv))
+      return fail(ZYFA_ERR_UNSUPPORTED, "internal: %d partial rows exceed the workspace bound", rows);
+    a.split_tiles = chunk;
+    a.part_o = static_cast<float*>(workspace);
+    const size_t rows_all = decode_partial_rows_bound(N, Hkv) * static_cast<size_t>(Hq);
+    a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows_all * 128 * 4 + 255) & ~size_t(255)));
+  }
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_decode_fp8 launch" : "attn_decode_bf16 launch");
+  if (a.split_tiles) {
+    e = zyfa::launch_decode_combine(a, ct, N, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "decode_combine launch");
+  }
   return ZYFA_OK;
 }
+
+size_t zyfa_decode_workspace_bytes(int N, int Hq, int Hkv) { return decode_ws_bytes(N, Hq, Hkv); }
 
 int zyfa_attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
                                 const int32_t* seq_lens, const int32_t* block_table, int64_t block_table_stride,
                                 int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                                 const int64_t q_strides[2], const int64_t k_cache_strides[3],
-                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
+                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* workspace,
+                                size_t workspace_bytes, void* stream) {
   return attn_decode(false, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, seq_lens, block_table,
                      block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
-                     v_cache_strides, o_strides, stream);
+                     v_cache_strides, o_strides, workspace, workspace_bytes, stream);
 }
 
 int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
@@ -691,10 +776,10 @@ int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void*
                                const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
                                int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                                const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
-                               const int64_t o_strides[2], void* stream) {
+                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, void* stream) {
   return attn_decode(true, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, seq_lens, block_table,
                      block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
-                     v_cache_strides, o_strides, stream);
+                     v_cache_strides, o_strides, workspace, workspace_bytes, stream);
 }
 
 static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,

@@ -126,6 +126,8 @@ struct Unit {
   bool has_b;
   int n_a, n_b, n_kv;
   int c0, dlt;             // paged K/V: cached tokens before the first query row = 128 c0 + dlt (else 0)
+  int j0;                  // decode step: first key block of the task (split key range), else 0
+  int part;                // decode step with split key ranges: partial-result row of the task, else -1
   int row0;                // first token of the sequence in the token dimension
   int len;                 // tokens of the sequence
   int sidx;                // sequence index of the scale arrays
@@ -163,6 +165,8 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
   w.n_kv = w.has_b ? w.n_b : w.n_a;
   w.c0 = 0;
   w.dlt = 0;
+  w.j0 = 0;
+  w.part = -1;
   w.row0 = 0;
   w.sidx = w.b;
   return w;
@@ -178,19 +182,40 @@ struct Sched {
   const Table* tab;
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
   bool one_token;          // decode step: one query token per sequence, its heads as tile rows
+  int split_tiles;         // decode step: nonzero when key ranges are split (per-sequence split counts in tab)
+  __device__ __forceinline__ int n_tasks() const {
+    return split_tiles ? tab->level_start[tab->n_seqs] : tab->n_seqs * Hkv;
+  }
   __device__ __forceinline__ int n_units() const {
-    if constexpr (VARLEN) return one_token ? (tab->n_seqs * Hkv + 1) / 2 : tab->level_start[tab->n_levels];
+    if constexpr (VARLEN) return one_token ? (n_tasks() + 1) / 2 : tab->level_start[tab->n_levels];
     else return B * Hq * (pair_hi - pair_lo);
   }
   // Decode step: task i = (sequence of rank i / Hkv, KV head i % Hkv), the
   // sequences longest first and KV heads adjacent; unit u runs tasks 2u (as
-  // tile A) and 2u + 1 (as tile B), each with its own K/V stream.
+  // tile A) and 2u + 1 (as tile B), each with its own K/V stream. With split
+  // key ranges a sequence of rank k owns tasks level_start[k] ..
+  // level_start[k+1] - 1, split-major (split s, head h at s * Hkv + h); its
+  // key blocks are cut into that many nearly equal splits, split s writing
+  // partial row ctx[k] + s.
   __device__ __forceinline__ Unit decode_task(int i, bool second) const {
-    const int rank = i / Hkv;
-    const int h = i - rank * Hkv;
+    int rank, s = 0;
+    if (split_tiles) {
+      int lo = 0, hi = tab->n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab->level_start[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      rank = lo;
+      i -= tab->level_start[rank];
+      s = i / Hkv;
+      i -= s * Hkv;
+    } else {
+      rank = i / Hkv;
+      i -= rank * Hkv;
+    }
     Unit w;
     w.b = 0;
-    w.hq = h * (Hq / Hkv);        // first query head of the group: tile row 0
+    w.hq = i * (Hq / Hkv);        // first query head of the group: tile row 0
     w.t = 0;
     w.row0 = tab->start[rank];    // the token's row in the packed queries
     w.len = tab->len[rank];       // keys, the new token's included
@@ -198,14 +223,26 @@ struct Sched {
     w.c0 = 0;
     w.dlt = 0;
     w.has_b = second;
-    w.n_a = w.n_b = w.n_kv = (w.len + 127) >> 7;
+    const int n_all = (w.len + 127) >> 7;
+    if (split_tiles) {
+      // the sequence's n_all key blocks in S nearly equal splits
+      const int S = (tab->level_start[rank + 1] - tab->level_start[rank]) / Hkv;
+      const int base = n_all / S, rem = n_all - base * S;
+      w.j0 = s * base + min(s, rem);
+      w.n_a = w.n_b = w.n_kv = base + (s < rem ? 1 : 0);
+      w.part = tab->ctx[rank] + s;
+    } else {
+      w.j0 = 0;
+      w.n_a = w.n_b = w.n_kv = n_all;
+      w.part = -1;
+    }
     return w;
   }
   // Tile B of a decode unit (call only when decode(u).has_b).
   __device__ __forceinline__ Unit decode_b(int u) const { return decode_task(2 * u + 1, true); }
   __device__ __forceinline__ Unit decode(int u) const {
     if constexpr (VARLEN) {
-      if (one_token) return decode_task(2 * u, 2 * u + 1 < tab->n_seqs * Hkv);
+      if (one_token) return decode_task(2 * u, 2 * u + 1 < n_tasks());
       // level k: the largest with level_start[k] <= u
       int lo = 0, hi = tab->n_levels - 1;
       while (lo < hi) {
@@ -222,6 +259,8 @@ struct Sched {
       w.len = tab->len[rank];
       w.sidx = tab->index[rank];
       const int ctx = tab->ctx[rank];
+      w.j0 = 0;
+      w.part = -1;
       w.c0 = ctx >> 7;
       w.dlt = ctx & 127;
       const int nq = (w.len + 127) / 128;
@@ -373,7 +412,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
             if (j >= (x ? nb : na)) continue;
             if ((j & 31) == 0) {
               const int e = j + lane;
-              pg[x] = e < wx.n_kv ? __ldg(a.block_table + wx.sidx * a.bt_stride + e) : 0;
+              pg[x] = e < wx.n_kv ? __ldg(a.block_table + wx.sidx * a.bt_stride + wx.j0 + e) : 0;
             }
             const int page = __shfl_sync(0xffffffffu, pg[x], j & 31);
             if (leader && (page < 0 || page >= a.num_pages)) atomicOr(a.status, kStatusBadPage);
@@ -927,7 +966,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         if (a.block_table) {
           if ((jj & 31) == 0) {
             const int e = jj + lane;
-            pages = e < n ? __ldg(a.block_table + w.sidx * a.bt_stride + e) : 0;
+            pages = e < n ? __ldg(a.block_table + w.sidx * a.bt_stride + w.j0 + e) : 0;
           }
           const int page = min(max(__shfl_sync(0xffffffffu, pages, jj & 31), 0), a.num_pages - 1);
           kv_i = static_cast<int64_t>(page) * a.Hkv + hkv;
@@ -980,8 +1019,9 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         diag = jd >= 0;
         lim = w.dlt + r - 128 * jd;
         if (sc.one_token) {          // every row is the token at position len - 1
-          diag = (j == n - 1);
-          lim = w.len - 1 - 128 * j;
+          const int ja = w.j0 + j;
+          diag = (ja == ((w.len - 1) >> 7));
+          lim = w.len - 1 - 128 * ja;
         }
       } else {
         diag = (j == n - 1);
@@ -1086,6 +1126,27 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     if (!__all_sync(0xffffffffu, ok)) { *abort_flag = 1; return; }
     oph ^= 1u;
     tc_fence_after();
+    if constexpr (VARLEN) {
+      if (w.part >= 0) {
+        // split key range: unnormalised O, the row's offset (or running
+        // maximum) m and its sum l, combined across splits afterwards
+        const int64_t prow = static_cast<int64_t>(w.part) * a.Hq + w.hq + r;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          __syncwarp();
+          tmem_ld32(tO + 32 * c, o);
+          if (r < group) {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(u2f(o[4 * e]), u2f(o[4 * e + 1]), u2f(o[4 * e + 2]), u2f(o[4 * e + 3]));
+          }
+        }
+        if (r < group) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m, l);
+        continue;
+      }
+    }
     const float inv = 1.f / l;
     const int q_row = qt * 128 + r;
     __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(w.row0 + q_row) * a.o_ss + w.hq * a.o_sh;
@@ -1139,6 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.pair_lo = a.pair_lo;
   sc.pair_hi = a.pair_hi;
   sc.one_token = a.one_token != 0;
+  sc.split_tiles = a.split_tiles;
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
@@ -1238,7 +1300,32 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
 }
 
 long long table_units(const AttnArgs& a, const SeqTable& tab) {
-  return a.one_token ? static_cast<long long>(tab.n_seqs) * a.Hkv : tab.level_start[tab.n_levels];
+  if (!a.one_token) return tab.level_start[tab.n_levels];
+  const long long tasks = a.split_tiles ? tab.level_start[tab.n_seqs] : static_cast<long long>(tab.n_seqs) * a.Hkv;
+  return (tasks + 1) / 2;
+}
+
+// Decode step with split key ranges: out = sum_s O_s 2^(m_s - M) /
+// sum_s l_s 2^(m_s - M), M = max_s m_s, for each (token, query head); one
+// block of 128 threads (one per output column) per (token, head).
+__global__ void __launch_bounds__(128) decode_combine_kernel(const float* __restrict__ part_o,
+                                                             const float2* __restrict__ part_ml,
+                                                             const __grid_constant__ CombineTable ct, int Hq,
+                                                             __nv_bfloat16* __restrict__ out, int64_t o_ss,
+                                                             int64_t o_sh) {
+  const int i = blockIdx.x / Hq, h = blockIdx.x - (blockIdx.x / Hq) * Hq;
+  const int base = ct.base[i], cnt = ct.count[i];
+  float mx = -INFINITY;
+  for (int s = 0; s < cnt; ++s) mx = fmaxf(mx, part_ml[static_cast<int64_t>(base + s) * Hq + h].x);
+  float acc = 0.f, den = 0.f;
+  for (int s = 0; s < cnt; ++s) {
+    const int64_t row = static_cast<int64_t>(base + s) * Hq + h;
+    const float2 ml = part_ml[row];
+    const float wgt = exp2f(ml.x - mx);
+    den = fmaf(ml.y, wgt, den);
+    acc = fmaf(part_o[row * 128 + threadIdx.x], wgt, acc);
+  }
+  out[static_cast<int64_t>(i) * o_ss + static_cast<int64_t>(h) * o_sh + threadIdx.x] = __float2bfloat16_rn(acc / den);
 }
 
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
@@ -1256,6 +1343,12 @@ cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& t
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_combine(const AttnArgs& a, const CombineTable& ct, int N, cudaStream_t stream) {
+  decode_combine_kernel<<<N * a.Hq, 128, 0, stream>>>(a.part_o, reinterpret_cast<const float2*>(a.part_ml), ct,
+                                                      a.Hq, static_cast<__nv_bfloat16*>(a.o), a.o_ss, a.o_sh);
+  return cudaGetLastError();
 }
 
 // Device-built tables: the unit count is only known on the device, so one

@@ -90,7 +90,21 @@ struct AttnArgs {
   // q map is over (token, head) rows, H = 1; tab.len holds each sequence's
   // key count (the new token included) and tab.start its token's row.
   int one_token;
+  // Decode step with split key ranges (split_tiles > 0): a task covers
+  // split_tiles key blocks and writes its rows' unnormalised O (fp32, Dv =
+  // 128) to part_o and (m, l) to part_ml (float pairs), row (p * Hq + head)
+  // for partial row p; decode_combine then writes o.
+  int split_tiles;
+  float* part_o;
+  float* part_ml;
 };
+
+// Partial rows of each sequence (caller's order) for decode_combine.
+struct CombineTable {
+  int base[kMaxVarlenSeqs];
+  int count[kMaxVarlenSeqs];
+};
+cudaError_t launch_decode_combine(const AttnArgs& a, const CombineTable& ct, int N, cudaStream_t stream);
 
 // A page index outside [0, num_pages): its keys read as zeros (the copy is
 // outside the tensor map) and its fp8 scales are taken from page 0 or the

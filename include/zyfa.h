@@ -326,8 +326,17 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  * attends to positions 0 .. seq_lens[i]-1. A task is (sequence, KV head):
  * the group's Hq/Hkv query heads are the rows of one 128-row tile, so K/V
  * are read once per KV head; each CTA runs two tasks as its two query tiles.
- * The results are the bytes of the paged prefill with ctx_lens[i] =
- * seq_lens[i] - 1 and one new token.
+ * Without a workspace the results are the bytes of the paged prefill with
+ * ctx_lens[i] = seq_lens[i] - 1 and one new token.
+ *
+ * workspace  : optional device memory (256-byte aligned) of at least
+ *              zyfa_decode_workspace_bytes(N, Hq, Hkv) bytes, owned by the
+ *              caller (calls that can run concurrently need their own). With
+ *              it, when the N*Hkv tasks would leave SMs idle, each task's key
+ *              range is split (at least 8 key blocks per split, about four
+ *              tasks per SM), every split writes its unnormalised rows with
+ *              their offset and sum, and a second kernel combines the splits
+ *              (results within rounding of the unsplit call). NULL: no split.
  *
  * q, o       : [N, Hq, Dqk|Dv]; q's token stride must be Hq x its head
  *              stride (each token's heads contiguous).
@@ -338,17 +347,19 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  *              [num_pages, Hkv].
  * Errors as the paged prefill.
  */
+size_t zyfa_decode_workspace_bytes(int N, int Hq, int Hkv);
 int zyfa_attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
                                 const int32_t* seq_lens, const int32_t* block_table, int64_t block_table_stride,
                                 int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                                 const int64_t q_strides[2], const int64_t k_cache_strides[3],
-                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
+                                const int64_t v_cache_strides[3], const int64_t o_strides[2], void* workspace,
+                                size_t workspace_bytes, void* stream);
 int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void* k_cache8, const float* k_scale,
                                const void* v_cache8, const float* v_scale, void* o, const int32_t* seq_lens,
                                const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
                                int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                                const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
-                               const int64_t o_strides[2], void* stream);
+                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -257,7 +257,8 @@ def _decode(L, lens, N, **kw):
     a.update(kw)
     return L.zyfa_attn_decode_bf16_paged(a["q"], a["kc"], a["vc"], a["o"], lens, a["bt"], a["bt_stride"],
                                          a["pages"], N, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"],
-                                         ctypes.c_float(a["scale"]), a["qs"], a["kcs"], a["vcs"], a["os_"], None)
+                                         ctypes.c_float(a["scale"]), a["qs"], a["kcs"], a["vcs"], a["os_"], None, 0,
+                                         None)
 
 
 @pytest.mark.parametrize("lens,N,kw,code", [
@@ -274,3 +275,10 @@ def _decode(L, lens, N, **kw):
 def test_decode_rejects_bad_arguments_on_host(L, lens, N, kw, code):
     assert _decode(L, lens, N, **kw) == code
     assert L.zyfa_last_error_message()
+
+
+def test_decode_workspace_size(L):
+    L.zyfa_decode_workspace_bytes.restype = ctypes.c_size_t
+    small = L.zyfa_decode_workspace_bytes(1, 32, 8)
+    big = L.zyfa_decode_workspace_bytes(64, 32, 8)
+    assert small > 0 and big > small and small % 4 == 0

@@ -218,7 +218,8 @@ def test_out_of_range_page_sets_the_status_and_reads_zeros():
 @pytest.mark.parametrize("fp8", [False, True])
 def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, fp8):
     """The decode call (query heads of a KV group as tile rows) against the
-    oracle, and byte for byte against the paged prefill with one new token."""
+    oracle, with and without split key ranges; without, byte for byte against
+    the paged prefill with one new token."""
     rng = np.random.default_rng(Hq + fp8)
     lens = [int(x) for x in rng.integers(1, 2500, size=13)] + [1, 2, 127, 128, 129, 256]
     seqs = [(L - 1, 1) for L in lens]
@@ -232,7 +233,8 @@ def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, fp8):
         q8, qs = zyfa.quantize_fp8_decode(qd)
         kc8, ks = zyfa.quantize_fp8_cache(kcd)
         vc8, vs = zyfa.quantize_fp8_cache(vcd)
-        o = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd)
+        o = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd, split=False)
+        o_split = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd)
         q8p, qsp = zyfa.quantize_fp8_varlen(qd, cu)
         ref_gpu = zyfa.attn_fwd_fp8_paged(q8p, qsp, kc8, ks, vc8, vs, cu, ctx, btd)
         zyfa.device_status()
@@ -242,11 +244,54 @@ def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, fp8):
         ko = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(kc), False))
         vo = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(vc), False))
     else:
-        o = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd)
+        o = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd, split=False)
+        o_split = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd)
         ref_gpu = zyfa.attn_fwd_bf16_paged(qd, kcd, vcd, cu, ctx, btd)
         zyfa.device_status()
         qo, ko, vo = f32(q), f32(kc), f32(vc)
     ref = np.concatenate([oattn.causal_attention_prefix(qo[i:i + 1], _gather(ko, btn[i], L), _gather(vo, btn[i], L),
                                                         1 / math.sqrt(D)) for i, L in enumerate(lens)])
-    (assert_fp8_gate if fp8 else assert_bf16_gate)(f32(o), ref, f"decode fp8={fp8} Hq={Hq} Hkv={Hkv}")
+    gate = assert_fp8_gate if fp8 else assert_bf16_gate
+    gate(f32(o), ref, f"decode fp8={fp8} Hq={Hq} Hkv={Hkv}")
+    gate(f32(o_split), ref, f"decode, split key ranges, fp8={fp8} Hq={Hq} Hkv={Hkv}")
     assert torch.equal(o, ref_gpu)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_small_batch_long_context_splits(fp8):
+    """Two sequences of 9000 and 20000 positions, 8 KV heads: 16 tasks for
+    the whole GPU, so the key ranges are split into many pieces; against the
+    oracle, and within rounding of the unsplit call. Queries are scaled by 3
+    so the rows attend to a few hundred keys rather than near-uniformly to
+    all 20000 (a flat average of random values shrinks the output to the
+    size of the FP8 probability-rounding noise, split or not)."""
+    lens = [9000, 20000]
+    seqs = [(L - 1, 1) for L in lens]
+    Hq, Hkv, D = 16, 8, 128
+    full = _sequences(seqs, Hq, Hkv, D, seed=41 + fp8)
+    full = [((q.float() * 3).to(torch.bfloat16), k, v) for q, k, v in full]
+    q, kc, vc, bt, cu = _paged(seqs, full)
+    qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
+    btn = bt.numpy()
+    if fp8:
+        q8, qs = zyfa.quantize_fp8_decode(qd)
+        kc8, ks = zyfa.quantize_fp8_cache(kcd)
+        vc8, vs = zyfa.quantize_fp8_cache(vcd)
+        o = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd)
+        o1 = zyfa.attn_decode_fp8_paged(q8, qs, kc8, ks, vc8, vs, lens, btd, split=False)
+        rq, rqs = ofp8.quantize_fp8_varlen(f32(q), cu, False)
+        qo = ofp8.dequantize_fp8_varlen(rq, rqs, cu)
+        ko = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(kc), False))
+        vo = ofp8.dequantize_fp8(*ofp8.quantize_fp8(f32(vc), False))
+    else:
+        o = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd)
+        o1 = zyfa.attn_decode_bf16_paged(qd, kcd, vcd, lens, btd, split=False)
+        qo, ko, vo = f32(q), f32(kc), f32(vc)
+    zyfa.device_status()
+    ref = np.concatenate([oattn.causal_attention_prefix(qo[i:i + 1], _gather(ko, btn[i], L), _gather(vo, btn[i], L),
+                                                        1 / math.sqrt(D)) for i, L in enumerate(lens)])
+    gate = assert_fp8_gate if fp8 else assert_bf16_gate
+    gate(f32(o), ref, f"decode split fp8={fp8}")
+    e_split = oattn.rel_l2(f32(o), ref)
+    e_one = oattn.rel_l2(f32(o1), ref)
+    assert e_split <= 1.25 * e_one + 1e-4, (e_split, e_one)
