@@ -214,16 +214,15 @@ def test_out_of_range_page_sets_the_status_and_reads_zeros():
 
 
 # ----------------------------------------------------------------- decode --
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (32, 1)])
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (4, 4, 128), (32, 1, 128), (4, 2, 192)])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, fp8):
+def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, D, fp8):
     """The decode call (query heads of a KV group as tile rows) against the
     oracle, with and without split key ranges; without, byte for byte against
     the paged prefill with one new token."""
     rng = np.random.default_rng(Hq + fp8)
     lens = [int(x) for x in rng.integers(1, 2500, size=13)] + [1, 2, 127, 128, 129, 256]
     seqs = [(L - 1, 1) for L in lens]
-    D = 128
     full = _sequences(seqs, Hq, Hkv, D, seed=31 + Hq + fp8)
     q, kc, vc, bt, cu = _paged(seqs, full)
     qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
