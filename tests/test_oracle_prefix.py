@@ -66,3 +66,40 @@ def test_future_key_is_masked_own_key_dominates():
     out = A.causal_attention_prefix(q, k, v, 1.0)
     np.testing.assert_allclose(out[0, 0, 0], np.arange(P + 1).mean(), rtol=1e-12)
     np.testing.assert_allclose(out[1:, 0, 0], P + 1, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- mutations --
+# Plausible mistakes planted in a local copy of the prefix oracle; a pin above
+# must tell each from the real one.
+
+def _prefix_mutant(q, k, v, scale, *, offset_shift=0, mask_by_query_index=False):
+    Lq, Hq, _ = q.shape
+    L, Hkv, _ = k.shape
+    P = L - Lq + offset_shift
+    pos = np.arange(Lq) if mask_by_query_index else P + np.arange(Lq)
+    allowed = np.arange(L)[None, :] <= pos[:, None]
+    out = np.empty((Lq, Hq, v.shape[2]))
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        s = np.where(allowed, (q[:, h] @ k[:, g].T) * scale, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:, h] = (p / p.sum(axis=1, keepdims=True)) @ v[:, g]
+    return out
+
+
+def _full_rows(q, k, v, scale, P):
+    return A.causal_attention(q[None], k[None], v[None], scale)[0][P:]
+
+
+def test_mutant_offset_by_one_is_caught():
+    q, k, v = _seq(19, seed=7)
+    ref = _full_rows(q, k, v, 0.3, 6)
+    np.testing.assert_allclose(A.causal_attention_prefix(q[6:], k, v, 0.3), ref, rtol=1e-12, atol=1e-14)
+    for shift in (-1, 1):
+        assert not np.allclose(_prefix_mutant(q[6:], k, v, 0.3, offset_shift=shift), ref)
+
+
+def test_mutant_mask_on_the_query_index_is_caught():
+    q, k, v = _seq(19, seed=8)
+    ref = _full_rows(q, k, v, 0.3, 6)
+    assert not np.allclose(_prefix_mutant(q[6:], k, v, 0.3, mask_by_query_index=True), ref)
