@@ -103,14 +103,14 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // box runs past the row and reads zeros, where a 5-D block would read the
 // next head (or past the tensor).
 int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elt, int D, int H, int S, int B,
-             const int64_t strides[3], const char* name) {
-  if ((D * elt) % 128 != 0) {
+             const int64_t strides[3], const char* name, int box_rows = 128) {
+  if ((D * elt) % 128 != 0 || box_rows != 128) {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(strides[2]) * elt,
                                     static_cast<cuuint64_t>(strides[1]) * elt,
                                     static_cast<cuuint64_t>(strides[0]) * elt};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), 1u, 128u, 1u};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), 1u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, gstrides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -601,7 +601,8 @@ constexpr int kMinSplitTiles = 8;
 constexpr int kMaxSmsForWorkspace = 256;
 
 static size_t decode_partial_rows_bound(int N, int Hkv) {
-  return static_cast<size_t>(kSplitTasksPerSm) * kMaxSmsForWorkspace / std::max(Hkv, 1) + 1 + std::max(N, 0);
+  // four copies of every split when the query rows are replicated
+  return 4 * (static_cast<size_t>(kSplitTasksPerSm) * kMaxSmsForWorkspace / std::max(Hkv, 1) + 1 + std::max(N, 0));
 }
 
 static size_t decode_ws_bytes(int N, int Hq, int Hkv) {
@@ -654,8 +655,10 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
   int r;
-  // q as rows of (token, head): the group of a KV head is 128 consecutive rows from its first head
-  if ((r = make_map(&tq, q, dt, elt, Dqk, 1, static_cast<int>(rows), 1, q3, "q")) ||
+  // q as rows of (token, head): the group of a KV head is consecutive rows
+  // from its first head; 32-row boxes when the rows are replicated
+  const bool replicate = workspace != nullptr && Hq / Hkv <= 32;
+  if ((r = make_map(&tq, q, dt, elt, Dqk, 1, static_cast<int>(rows), 1, q3, "q", replicate ? 32 : 128)) ||
       (r = make_map(&tk, kc, dt, elt, Dqk, Hkv, 128, num_pages, kcs, "k_cache")) ||
       (r = make_map(&tv, vc, dt, elt, Dv, Hkv, 128, num_pages, vcs, "v_cache")))
     return r;
@@ -721,29 +724,32 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
         rows += (n + c - 1) / c;
       }
       if (!any) break;
-      if (rows > decode_partial_rows_bound(N, Hkv)) continue;   // more partial rows than the workspace holds
+      if ((Hq / Hkv <= 32 ? 4 : 1) * rows > decode_partial_rows_bound(N, Hkv)) continue;   // beyond the workspace
       const int64_t m = makespan(c);
       if (m < best) { best = m; chunk = c; }
     }
   }
-  if (chunk) {
+  if (chunk || replicate) {
     if (!aligned(workspace, 256)) return fail(ZYFA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     if (workspace_bytes < decode_ws_bytes(N, Hq, Hkv))
       return fail(ZYFA_ERR_INVALID_ARG, "workspace of %zu bytes is below zyfa_decode_workspace_bytes = %zu",
                   workspace_bytes, decode_ws_bytes(N, Hq, Hkv));
+    const int copies = replicate ? 4 : 1;
     int rows = 0;
     for (int k = 0; k < N; ++k) {
-      const int splits = ((tab.len[k] + 127) / 128 + chunk - 1) / chunk;   // each at least chunk/2 blocks
+      // splits of at least chunk/2 blocks each (one without a split)
+      const int splits = chunk ? ((tab.len[k] + 127) / 128 + chunk - 1) / chunk : 1;
       tab.level_start[k] = rows * Hkv;
       tab.ctx[k] = rows;
-      ct.base[tab.index[k]] = rows;
-      ct.count[tab.index[k]] = splits;
+      ct.base[tab.index[k]] = copies * rows;
+      ct.count[tab.index[k]] = copies * splits;
       rows += splits;
     }
     tab.level_start[N] = rows * Hkv;
-    if (static_cast<size_t>(rows) > decode_partial_rows_bound(N, Hkv))
-      return fail(ZYFA_ERR_UNSUPPORTED, "internal: %d partial rows exceed the workspace bound", rows);
-    a.split_tiles = chunk;
+    if (static_cast<size_t>(copies) * rows > decode_partial_rows_bound(N, Hkv))
+      return fail(ZYFA_ERR_UNSUPPORTED, "internal: %d partial rows exceed the workspace bound", copies * rows);
+    a.split_tiles = 1;
+    a.replicate = replicate ? 1 : 0;
     a.part_o = static_cast<float*>(workspace);
     const size_t rows_all = decode_partial_rows_bound(N, Hkv) * static_cast<size_t>(Hq);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows_all * 128 * 4 + 255) & ~size_t(255)));

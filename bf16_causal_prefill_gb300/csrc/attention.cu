@@ -347,7 +347,7 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 // and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
-template <int DQK, bool FP8, int STREAM, bool VARLEN>
+template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE = false>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
                             const AttnArgs& a, const Sched<VARLEN>& sc, bool leader) {
   using C = Cfg<DQK, FP8>;
@@ -386,6 +386,15 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
               row = x.row0 * a.Hq + x.hq;
               qh = 0;
             }
+          }
+          if constexpr (SLICE) {
+            // the group's rows four times, at tile rows 0, 32, 64, 96
+            // (32-row boxes per 128-byte column block)
+            for (int cpy = 0; cpy < 4; ++cpy)
+#pragma unroll
+              for (int kb = 0; kb < C::kQkBlocks; ++kb)
+                tma_load_4d(sm.q_tile(qt) + kb * 16384 + cpy * 4096, tm_q, sm.q_full(), kb * C::kInnerElts, 0, row, 0);
+            continue;
           }
           if constexpr (C::kQkWhole) {
             tma_load_5d(sm.q_tile(qt), tm_q, sm.q_full(), 0, row, 0, qh, w.b);
@@ -911,7 +920,78 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float rho) {
 // with no measurable change in the output error.
 constexpr float kWinLo = -4.0f, kWinHi = 8.0f, kWinCentre = 0.0f, kFloorBinades = 64.0f;
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN>
+// Decode step with replicated query rows (the SLICE kernels): warp c of a
+// softmax warpgroup holds a copy of the group's rows and takes key columns
+// 32c .. 32c + 31 of every block (the other columns of its P are zero), with
+// its own offset (or running maximum), sum and O rows; the four copies are
+// combined like split key ranges. Same arithmetic per column as the
+// full-row pass. A copy can see no key at all (a short sequence's last
+// block): it keeps m = -inf, l = 0 and O = 0, which the combine weighs 0.
+template <bool FP8>
+__device__ __forceinline__ void slice_probs(uint32_t tS, uint32_t tO, int cpy, bool diag, int lim, bool first,
+                                            float cj, float lsv, float& m, float& l, float& top, uint32_t (&pk)[FP8 ? 32 : 64],
+                                            float& psum) {
+  uint32_t s[32];
+  tmem_ld32(tS + 32 * cpy, s);
+  if (diag) mask_chunk(s, 32 * cpy, lim);
+  float a8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a8[i] = max3f(u2f(s[i]), u2f(s[8 + i]), fmaxf(u2f(s[16 + i]), u2f(s[24 + i])));
+  const float mx = max3f(max3f(a8[0], a8[1], a8[2]), max3f(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7]));
+  constexpr int kW = FP8 ? 8 : 16;     // P words of one 32-column slice
+  uint32_t pw[kW];
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  bool moved = false;
+  float rho = 1.f;
+  if constexpr (FP8) {
+    const float bm = mx * cj + lsv;
+    if (first) {
+      top = bm;
+      m = top - kWinCentre;
+    } else {
+      const float rel = bm - m;
+      const bool need = rel > kWinHi || (rel < kWinLo && bm > top - kFloorBinades);
+      const float m_new = need ? fmaxf(bm - kWinCentre, fmaxf(top, bm) - kFloorBinades) : m;
+      top = fmaxf(top, bm);
+      moved = __any_sync(0xffffffffu, need);
+      if (moved) {
+        rho = ex2_approx(m - m_new);
+        l *= rho;
+        m = m_new;
+      }
+    }
+    // a copy whose columns are all hidden so far keeps m = -inf (its
+    // probabilities are 0, its partial row is empty); the exponent offset
+    // must stay finite there
+    probs_chunk<true>(0, s, cj, lsv - (m == -INFINITY ? 0.f : m), pw, acc);
+  } else {
+    const float xmax = mx * cj;
+    if (first) {
+      m = xmax;
+    } else {
+      const bool need = xmax > m + kRescaleThreshold;
+      moved = __any_sync(0xffffffffu, need);
+      if (moved) {
+        const float m_new = need ? xmax : m;
+        rho = ex2_approx(m - m_new);
+        l *= rho;
+        m = m_new;
+      }
+    }
+    probs_chunk<false>(0, s, cj, m == -INFINITY ? 0.f : -m, pw, acc);
+  }
+  // the slice's words at its columns, zeros elsewhere (static indices keep
+  // pk in registers)
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < kW; ++i) pk[kW * c + i] = (c == cpy) ? pw[i] : 0u;
+  const float2 t = __fadd2_rn(acc[0], acc[1]);
+  psum = t.x + t.y;
+  if (moved) rescale_o_row(tO, rho);
+}
+
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE = false>
 __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
                              int warp, int lane) {
   const int n_units = sc.n_units();
@@ -951,7 +1031,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       int64_t qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt;
       if constexpr (VARLEN) {
         // decode step: row r is query head hq + r, with its own scale
-        if (sc.one_token) qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq + min(r, group - 1)) * nblk;
+        if (sc.one_token) qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq + min(SLICE ? (r & 31) : r, group - 1)) * nblk;
       }
       sq = __ldg(a.q_scale + qi);
       kv_scale_row = (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
@@ -974,10 +1054,10 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       }
       return kv_i;
     };
-    // Packed and paged inputs load the next block's scales one tile ahead
-    // (in a decode step S is often ready before these loads would return).
+    // Decode steps with replicated rows load the next block's scales one
+    // tile ahead (S is often ready before these loads would return).
     float sk_next = 0.f, sv_next = 0.f;
-    if constexpr (FP8 && VARLEN) {
+    if constexpr (FP8 && SLICE) {
       const int64_t i0 = kv_index(0);
       sk_next = __ldg(a.k_scale + i0);
       sv_next = __ldg(a.v_scale + i0);
@@ -986,7 +1066,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       float cj = a.scale_log2, lsv = 0.f, inv_sv = 1.f;
       if constexpr (FP8) {
         float sk, sv;
-        if constexpr (VARLEN) {
+        if constexpr (SLICE) {
           sk = sk_next;
           sv = sv_next;
           if (j + 1 < n) {
@@ -1030,7 +1110,9 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       uint32_t pk[kPk];
       float psum = 0.f;
       const bool first = (j == 0);
-      if constexpr (FP8) {
+      if constexpr (SLICE) {
+        slice_probs<FP8>(tS, tO, warp & 3, diag, lim, first, cj, lsv, m, l, top, pk, psum);
+      } else if constexpr (FP8) {
         // The whole row of S in one load and its maximum first: the offset is
         // set (first tile) or moved (a tile whose largest P' would leave the
         // window) before any exponential, so no tile computes them twice.
@@ -1130,20 +1212,22 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       if (w.part >= 0) {
         // split key range: unnormalised O, the row's offset (or running
         // maximum) m and its sum l, combined across splits afterwards
-        const int64_t prow = static_cast<int64_t>(w.part) * a.Hq + w.hq + r;
+        // replicated rows: copy c of row i is partial row 4 part + c, head hq + i
+        const int rr = SLICE ? (r & 31) : r;
+        const int64_t prow = static_cast<int64_t>(SLICE ? 4 * w.part + (warp & 3) : w.part) * a.Hq + w.hq + rr;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           __syncwarp();
           tmem_ld32(tO + 32 * c, o);
-          if (r < group) {
+          if (rr < group) {
             float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               dst[e] = make_float4(u2f(o[4 * e]), u2f(o[4 * e + 1]), u2f(o[4 * e + 2]), u2f(o[4 * e + 3]));
           }
         }
-        if (r < group) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m, l);
+        if (rr < group) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m, l);
         continue;
       }
     }
@@ -1176,7 +1260,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8, bool VARLEN, bool LEAN>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
@@ -1234,16 +1318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK>(sm, &tm_q, &tm_k, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE>(sm, &tm_q, &tm_k, a, sc, leader);
     } else if (warp == kLoadWarpV) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV>(sm, &tm_q, &tm_v, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE>(sm, &tm_q, &tm_v, a, sc, leader);
     } else if (warp == kMmaWarp) {
       mma_role(sm, tmem, a, sc, leader);
     }
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role<DQK, FP8, VARLEN, LEAN>(sm, tmem, a, sc, warp, lane);
+    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE>(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -1254,12 +1338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN = false>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                    const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream,
                    const typename Sched<VARLEN>::Table* tab_global = nullptr) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE>;
   // The shared-memory opt-in is per function and device: set it once.
   static bool opted_in[64] = {};
   int dev = 0;
@@ -1331,6 +1415,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __rest
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
   const long long n = table_units(a, tab);
+  if (a.replicate && a.Dqk == 128) return launch<128, false, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.replicate && a.Dqk == 192) return launch<192, false, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;
@@ -1339,6 +1425,8 @@ cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& 
 cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                    const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
   const long long n = table_units(a, tab);
+  if (a.replicate && a.Dqk == 128) return launch<128, true, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.replicate && a.Dqk == 192) return launch<192, true, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);

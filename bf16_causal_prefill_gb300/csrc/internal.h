@@ -97,6 +97,11 @@ struct AttnArgs {
   int split_tiles;
   float* part_o;
   float* part_ml;
+  // Decode step, groups of at most 32 heads, with partial rows: the q map's
+  // box is 32 rows, loaded at tile rows 0, 32, 64 and 96; warp c of a softmax
+  // warpgroup takes key columns 32c .. 32c + 31 and writes partial row
+  // 4 p + c for the task's partial row p (a separate kernel instantiation).
+  int replicate;
 };
 
 // Partial rows of each sequence (caller's order) for decode_combine.
