@@ -334,9 +334,12 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  *              caller (calls that can run concurrently need their own). With
  *              it, when the N*Hkv tasks would leave SMs idle, each task's key
  *              range is split (at least 8 key blocks per split, about four
- *              tasks per SM), every split writes its unnormalised rows with
- *              their offset and sum, and a second kernel combines the splits
- *              (results within rounding of the unsplit call). NULL: no split.
+ *              tasks per SM), and with Hq/Hkv <= 32 the group's rows are
+ *              replicated four times in the tile so that each softmax warp
+ *              takes a quarter of every key block's columns; every split and
+ *              copy writes its unnormalised rows with their offset and sum,
+ *              and a second kernel combines them (results within rounding of
+ *              the call without a workspace). NULL: neither.
  *
  * q, o       : [N, Hq, Dqk|Dv]; q's token stride must be Hq x its head
  *              stride (each token's heads contiguous).
