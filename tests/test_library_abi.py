@@ -282,3 +282,20 @@ def test_decode_workspace_size(L):
     small = L.zyfa_decode_workspace_bytes(1, 32, 8)
     big = L.zyfa_decode_workspace_bytes(64, 32, 8)
     assert small > 0 and big > small and small % 4 == 0
+
+
+def test_python_paged_and_decode_bindings_check_tensors_before_any_launch():
+    # CPU tensors (and a wrong dtype) are refused in the binding, before the
+    # library is called
+    import torch
+    q = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    cache = torch.zeros(3, 128, 1, 128, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 3, dtype=torch.int32)
+    with pytest.raises(ValueError):                       # CPU tensors
+        zyfa.attn_fwd_bf16_paged(q, cache, cache, [0, 2, 4], [0, 0], bt)
+    with pytest.raises(ValueError):
+        zyfa.attn_decode_bf16_paged(q, cache, cache, [5, 5, 5, 5], torch.zeros(4, 3, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        zyfa.quantize_fp8_cache(torch.zeros(3, 64, 1, 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        zyfa.quantize_fp8_decode(torch.zeros(4, 2, 128, dtype=torch.float32))
