@@ -7,6 +7,12 @@
  * probabilities, normalisation by the rounded row sum, and an optional
  * 128-point Hadamard rotation of Q and K before quantisation.
  *
+ * Entry points: the quantiser and the two attention calls on [B, S, H, D]
+ * batches (plus query-row ranges and a prefill from page-locked host
+ * memory); the same on packed variable-length batches (offsets on the host
+ * or on the device); packed queries that continue cached sequences over a
+ * paged K/V cache; and a decode step over that cache.
+ *
  * Sources of the operations (page title, section):
  *   - "ZYFA: Fast and Accurate FP8 Attention on AMD MI355X": "Introduction"
  *     and "Methodology and Limitations" (causal forward pass, equal query and
