@@ -90,6 +90,11 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8_varlen_dev.restype = c_int
     L.zyfa_attn_fwd_fp8_varlen_dev.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                                c_int, c_int, c_float, vp, vp, vp, vp, vp, vp]
+    L.zyfa_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    L.zyfa_noalloc_scratch_bytes.argtypes = []
+    L.zyfa_attn_fwd_fp8_varlen_dev_noalloc.restype = c_int
+    L.zyfa_attn_fwd_fp8_varlen_dev_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                                       c_int, c_int, c_int, c_float, vp, vp, vp, vp, vp]
     L.zyfa_quantize_fp8_varlen.restype = c_int
     L.zyfa_quantize_fp8_varlen.argtypes = [vp, i64, i64, vp, vp, vp, c_int, c_int, c_int, c_int, vp]
     L.zyfa_attn_fwd_bf16_varlen.restype = c_int
@@ -440,6 +445,42 @@ def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
                                           v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, B, Hq, Hkv, Dqk,
                                           Dv, float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
                                           _strides2(out), _stream_ptr(q8, stream)))
+    return out
+
+
+def attn_fwd_fp8_varlen_dev_noalloc(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor,
+                                    k_scale: torch.Tensor, v8: torch.Tensor, v_scale: torch.Tensor,
+                                    cu_seqlens: torch.Tensor, max_seqlen: int, out: torch.Tensor,
+                                    softmax_scale: Optional[float] = None,
+                                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """attn_fwd_fp8_varlen with device offsets for callers that cannot
+    allocate device memory on the call path (a replayed CUDA graph with fixed
+    memory, a serving loop drawing only from its own pool): the library keeps
+    the call's unit table in a static 32 KB device array instead of a
+    workspace, so neither this function nor the library allocates; the caller
+    passes every input and the output `out` [T,Hq,Dv] bf16. Calls that can
+    overlap on the GPU share that array and must not be issued concurrently.
+    Results are bitwise those of attn_fwd_fp8_varlen(..., max_seqlen=...)."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _require_packed(t, n, torch.uint8)
+    _require_packed(out, "out", torch.bfloat16)
+    T, Hq, Dqk = q8.shape
+    Hkv, Dv = k8.shape[1], v8.shape[2]
+    dev = _cu_device(cu_seqlens, max_seqlen, q8.device)
+    if dev is None:
+        raise ValueError("cu_seqlens must be an int32 CUDA tensor and max_seqlen must be given")
+    cu_ptr, B, max_len = dev
+    nb = scale_blocks(max_len)
+    for t, n, h in ((q_scale, "q_scale", Hq), (k_scale, "k_scale", Hkv), (v_scale, "v_scale", Hkv)):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, h, nb):
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor [B, H, ceil(max_seqlen/128)]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dqk)
+    _check(lib().zyfa_attn_fwd_fp8_varlen_dev_noalloc(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(),
+                                                      k_scale.data_ptr(), v8.data_ptr(), v_scale.data_ptr(),
+                                                      out.data_ptr(), cu_ptr, B, T, max_len, Hq, Hkv, Dqk, Dv,
+                                                      float(softmax_scale), _strides2(q8), _strides2(k8),
+                                                      _strides2(v8), _strides2(out), _stream_ptr(q8, stream)))
     return out
 
 

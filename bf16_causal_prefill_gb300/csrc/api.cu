@@ -896,6 +896,68 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
                      workspace);
 }
 
+// ----------------------------- packed FP8 attention without a workspace
+// For callers that cannot allocate device memory on the call path: a step
+// replayed inside a CUDA graph whose memory was fixed at capture, a serving
+// loop that hands out memory only from its own pool, or a process that runs
+// with the allocator locked. zyfa_attn_fwd_fp8_varlen_dev needs a caller
+// workspace for the unit table its first kernel builds; this form keeps that
+// table in one array of this file instead. The array holds one table for up
+// to kMaxVarlenSeqs sequences of up to 2 * 128 * kMaxVarlenLevels tokens
+// (check_dev_seqlens rejects anything larger), stays resident on every device
+// that loads the library until the process exits, and is shared by all calls:
+// each call rewrites every field the attention kernel reads, and calls whose
+// kernels overlap on the GPU race on it.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 32768;
+static_assert(sizeof(zyfa::SeqTable) <= kNoAllocScratchBytes, "the unit table must fit the static scratch");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device (the host-side
+// symbol is only a stand-in). Looked up once per device, with that device
+// current, on the first call there.
+int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(ZYFA_ERR_UNSUPPORTED, "device ordinal %d outside 0..63", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(static scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return ZYFA_OK;
+}
+}  // namespace
+
+size_t zyfa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int zyfa_attn_fwd_fp8_varlen_dev_noalloc(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                                         const void* v8, const float* v_scale, void* o,
+                                         const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen,
+                                         int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                                         const int64_t q_strides[2], const int64_t k_strides[2],
+                                         const int64_t v_strides[2], const int64_t o_strides[2], void* stream) {
+  // The static table bounds the batch: refuse what it cannot hold before
+  // touching the device.
+  if (B < 1 || B > zyfa::kMaxVarlenSeqs)
+    return fail(ZYFA_ERR_INVALID_ARG, "batch %d outside 1..%d (the static scratch holds one table of at most %d sequences)",
+                B, zyfa::kMaxVarlenSeqs, zyfa::kMaxVarlenSeqs);
+  if (max_seqlen > 2 * 128 * zyfa::kMaxVarlenLevels)
+    return fail(ZYFA_ERR_UNSUPPORTED, "max_seqlen %d exceeds %d (the static scratch holds one table of sequences up to that length)",
+                max_seqlen, 2 * 128 * zyfa::kMaxVarlenLevels);
+  void* scratch = nullptr;
+  if (int r = noalloc_scratch(&scratch)) return r;
+  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
+                     scratch);
+}
+
 // ------------------------------------------------ prefill from host memory
 // Per-device copy streams and per-chunk events of the host pipeline.
 namespace {

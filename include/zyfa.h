@@ -279,6 +279,39 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
                                  void* stream);
 
 /*
+ * zyfa_attn_fwd_fp8_varlen_dev without a workspace: an addition of this
+ * library with no counterpart on the pages. It is meant for callers that
+ * cannot allocate device memory where they call attention: a step replayed
+ * from a CUDA graph whose memory was fixed when it was captured, a serving
+ * loop that hands out device memory only from its own pool, or a process that
+ * runs with its allocator locked. The unit table that the workspace form
+ * builds in caller memory lives instead in one static array of the library
+ * (zyfa_noalloc_scratch_bytes() = 32 KB, 256-byte aligned), so this call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call);
+ * the caller still owns every input and output.
+ *
+ * Limits and sharing: the array holds the table of at most 1024 sequences of
+ * at most 262144 tokens each; B outside 1..1024 returns ZYFA_ERR_INVALID_ARG
+ * and a larger max_seqlen ZYFA_ERR_UNSUPPORTED, before anything is enqueued.
+ * The array is resident on every GPU that loads the library until the
+ * process exits. All calls share it and each call rewrites it in full, so two
+ * calls whose kernels can overlap on the GPU (different streams without an
+ * ordering between them) race on it; calls on one stream are safe. The first
+ * call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.
+ *
+ * Arguments, results (bitwise those of zyfa_attn_fwd_fp8_varlen_dev) and the
+ * other errors as zyfa_attn_fwd_fp8_varlen_dev, without the workspace.
+ */
+size_t zyfa_noalloc_scratch_bytes(void);
+int zyfa_attn_fwd_fp8_varlen_dev_noalloc(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                                         const void* v8, const float* v_scale, void* o,
+                                         const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen,
+                                         int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
+                                         const int64_t q_strides[2], const int64_t k_strides[2],
+                                         const int64_t v_strides[2], const int64_t o_strides[2], void* stream);
+
+/*
  * Packed queries over a PAGED K/V cache: chunked prefill and prefix caching.
  * The pages name paged K/V as future work ("ZYFA ...", "Methodology and
  * Limitations"); this is the cache layout serving stacks use. Sequence i

@@ -299,3 +299,19 @@ def test_python_paged_and_decode_bindings_check_tensors_before_any_launch():
         zyfa.quantize_fp8_cache(torch.zeros(3, 64, 1, 128, dtype=torch.bfloat16))
     with pytest.raises(ValueError):
         zyfa.quantize_fp8_decode(torch.zeros(4, 2, 128, dtype=torch.float32))
+
+
+def test_noalloc_call_refuses_what_its_static_table_cannot_hold(L):
+    # the static scratch holds one unit table: at most 1024 sequences of at
+    # most 262144 tokens; larger calls fail on the host before any device work
+    assert L.zyfa_noalloc_scratch_bytes() == 32768
+    s2 = (ctypes.c_int64 * 2)(128, 128)
+    def call(B, max_len):
+        return L.zyfa_attn_fwd_fp8_varlen_dev_noalloc(16, 16, 16, 16, 16, 16, 16, 16, B, 1000, max_len, 1, 1, 128,
+                                                       128, ctypes.c_float(0.1), s2, s2, s2, s2, None)
+    assert call(2000, 1000) == 1
+    assert b"static scratch" in L.zyfa_last_error_message()
+    assert call(0, 1000) == 1
+    assert call(4, 300000) == 2
+    assert b"static scratch" in L.zyfa_last_error_message()
+
