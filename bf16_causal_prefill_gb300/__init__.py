@@ -609,13 +609,19 @@ def _decode_meta(seq_lens, block_table: torch.Tensor, N: int, device):
 
 def _decode_workspace(N: int, Hq: int, Hkv: int, device, split, stream):
     """(pointer, bytes, tensor) of the split-key-range workspace: split=True
-    allocates one, a uint8 CUDA tensor is used as given, False/None gives none."""
+    allocates one, a uint8 CUDA tensor is used as given, False/None gives none.
+    split=True allocates nothing when the library would use the workspace for
+    neither a split (considered only while N*Hkv < 4 x the SM count) nor
+    replicated rows (groups of at most 32 query heads)."""
     if split is False or split is None:
         return None, 0, None
     if isinstance(split, torch.Tensor):
         if not split.is_cuda or split.dtype != torch.uint8:
             raise ValueError("workspace must be a uint8 CUDA tensor")
         return split.data_ptr(), split.numel(), split
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if Hq // Hkv > 32 and N * Hkv >= 4 * sms:
+        return None, 0, None
     ws = torch.empty(lib().zyfa_decode_workspace_bytes(N, Hq, Hkv), dtype=torch.uint8, device=device)
     if stream is not None:
         ws.record_stream(stream)

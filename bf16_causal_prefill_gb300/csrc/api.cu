@@ -600,14 +600,18 @@ constexpr int kSplitTasksPerSm = 4;
 constexpr int kMinSplitTiles = 8;
 constexpr int kMaxSmsForWorkspace = 256;
 
-static size_t decode_partial_rows_bound(int N, int Hkv) {
-  // four copies of every split when the query rows are replicated
-  return 4 * (static_cast<size_t>(kSplitTasksPerSm) * kMaxSmsForWorkspace / std::max(Hkv, 1) + 1 + std::max(N, 0));
+// Query rows are replicated (four copies of every split) for groups of at
+// most 32 query heads per KV head; larger groups keep one copy.
+static int decode_copies(int Hq, int Hkv) { return Hkv >= 1 && Hq / Hkv <= 32 ? 4 : 1; }
+
+static size_t decode_partial_rows_bound(int N, int Hq, int Hkv) {
+  return decode_copies(Hq, Hkv) *
+         (static_cast<size_t>(kSplitTasksPerSm) * kMaxSmsForWorkspace / std::max(Hkv, 1) + 1 + std::max(N, 0));
 }
 
 static size_t decode_ws_bytes(int N, int Hq, int Hkv) {
   // per partial row and head: 128 fp32 of O and (m, l)
-  const size_t rows = decode_partial_rows_bound(N, Hkv) * static_cast<size_t>(std::max(Hq, 0));
+  const size_t rows = decode_partial_rows_bound(N, Hq, Hkv) * static_cast<size_t>(std::max(Hq, 0));
   return ((rows * 128 * 4 + 255) & ~size_t(255)) + rows * 2 * 4;
 }
 
@@ -724,7 +728,7 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
         rows += (n + c - 1) / c;
       }
       if (!any) break;
-      if ((Hq / Hkv <= 32 ? 4 : 1) * rows > decode_partial_rows_bound(N, Hkv)) continue;   // beyond the workspace
+      if (decode_copies(Hq, Hkv) * rows > decode_partial_rows_bound(N, Hq, Hkv)) continue;   // beyond the workspace
       const int64_t m = makespan(c);
       if (m < best) { best = m; chunk = c; }
     }
@@ -746,12 +750,12 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
       rows += splits;
     }
     tab.level_start[N] = rows * Hkv;
-    if (static_cast<size_t>(copies) * rows > decode_partial_rows_bound(N, Hkv))
+    if (static_cast<size_t>(copies) * rows > decode_partial_rows_bound(N, Hq, Hkv))
       return fail(ZYFA_ERR_UNSUPPORTED, "internal: %d partial rows exceed the workspace bound", copies * rows);
     a.split_tiles = 1;
     a.replicate = replicate ? 1 : 0;
     a.part_o = static_cast<float*>(workspace);
-    const size_t rows_all = decode_partial_rows_bound(N, Hkv) * static_cast<size_t>(Hq);
+    const size_t rows_all = decode_partial_rows_bound(N, Hq, Hkv) * static_cast<size_t>(Hq);
     a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows_all * 128 * 4 + 255) & ~size_t(255)));
   }
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8_varlen(tq, tk, tv, a, tab, static_cast<cudaStream_t>(stream))

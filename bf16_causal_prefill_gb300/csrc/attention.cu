@@ -176,18 +176,21 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
 // (decode_unit). Packed variable lengths: the host-built level table.
 struct NoTable {};
 
-template <bool VARLEN>
+// DECODE: the kernel instantiation runs decode steps (one query token per
+// sequence); prefill instantiations compile none of that code.
+template <bool VARLEN, bool DECODE = false>
 struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
-  bool one_token;          // decode step: one query token per sequence, its heads as tile rows
+  bool one_token;          // decode step: one query token per sequence, its heads as tile rows (DECODE only)
+  __device__ __forceinline__ bool step() const { return DECODE && one_token; }
   int split_tiles;         // decode step: nonzero when key ranges are split (per-sequence split counts in tab)
   __device__ __forceinline__ int n_tasks() const {
     return split_tiles ? tab->level_start[tab->n_seqs] : tab->n_seqs * Hkv;
   }
   __device__ __forceinline__ int n_units() const {
-    if constexpr (VARLEN) return one_token ? (n_tasks() + 1) / 2 : tab->level_start[tab->n_levels];
+    if constexpr (VARLEN) return step() ? (n_tasks() + 1) / 2 : tab->level_start[tab->n_levels];
     else return B * Hq * (pair_hi - pair_lo);
   }
   // Decode step: task i = (sequence of rank i / Hkv, KV head i % Hkv), the
@@ -242,7 +245,7 @@ struct Sched {
   __device__ __forceinline__ Unit decode_b(int u) const { return decode_task(2 * u + 1, true); }
   __device__ __forceinline__ Unit decode(int u) const {
     if constexpr (VARLEN) {
-      if (one_token) return decode_task(2 * u, 2 * u + 1 < n_tasks());
+      if (step()) return decode_task(2 * u, 2 * u + 1 < n_tasks());
       // level k: the largest with level_start[k] <= u
       int lo = 0, hi = tab->n_levels - 1;
       while (lo < hi) {
@@ -347,9 +350,9 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 // and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
-template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE = false>
+template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE, bool DECODE>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
-                            const AttnArgs& a, const Sched<VARLEN>& sc, bool leader) {
+                            const AttnArgs& a, const Sched<VARLEN, DECODE>& sc, bool leader) {
   using C = Cfg<DQK, FP8>;
   constexpr bool kIsK = (STREAM == kStreamQK);
   constexpr int kStages = kIsK ? C::kNK : C::kNV;
@@ -381,7 +384,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
           if constexpr (VARLEN) {
             // decode step: the map is over (token, head) rows; a group's
             // heads are consecutive rows; tile B holds the second task
-            if (sc.one_token) {
+            if (sc.step()) {
               const Unit x = qt ? sc.decode_b(u) : w;
               row = x.row0 * a.Hq + x.hq;
               qh = 0;
@@ -408,7 +411,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
       ++qn;
     }
     if constexpr (VARLEN) {
-      if (sc.one_token) {
+      if (sc.step()) {
         // Decode step: the two tasks' key blocks alternate in the ring
         // (A0, B0, A1, B1, ...; a finished task drops out), the order in
         // which the MMA warp consumes them.
@@ -539,8 +542,8 @@ __device__ __forceinline__ void issue_pv(const OperandDescs& od, uint32_t tmem_p
 // The whole warp runs the schedule (waits, stage and phase bookkeeping,
 // descriptors: all warp-uniform); one elected lane issues tcgen05.mma and
 // tcgen05.commit, so a commit tracks exactly the MMAs of that lane.
-template <int DQK, bool FP8, bool VARLEN>
-__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool DECODE>
+__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, DECODE>& sc,
                          bool leader) {
   using C = Cfg<DQK, FP8>;
   const int n_units = sc.n_units();
@@ -572,7 +575,7 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
       ZYFA_WAIT(sm.q_full(), qn & 1u);
       ++qn;
       if constexpr (VARLEN) {
-        if (sc.one_token) {
+        if (sc.step()) {
           // Decode step: tasks A and B of the unit are independent chains
           // (own K/V blocks, interleaved in the rings), ping-ponged like two
           // query tiles: S_A(0), S_B(0), then per block PV_X(j), S_X(j+1).
@@ -991,8 +994,8 @@ __device__ __forceinline__ void slice_probs(uint32_t tS, uint32_t tO, int cpy, b
   if (moved) rescale_o_row(tO, rho);
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE = false>
-__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool DECODE>
+__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, DECODE>& sc,
                              int warp, int lane) {
   const int n_units = sc.n_units();
   const int nblk = a.scale_blocks;
@@ -1015,7 +1018,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
     if constexpr (VARLEN) {
-      if (sc.one_token && wg == 1) w = sc.decode_b(u);   // decode step: tile B runs the unit's second task
+      if (sc.step() && wg == 1) w = sc.decode_b(u);   // decode step: tile B runs the unit's second task
     }
     const int qt = 2 * w.t + wg;
     const int n = wg ? w.n_b : w.n_a;   // key blocks this query tile sees
@@ -1031,7 +1034,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
       int64_t qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq) * nblk + qt;
       if constexpr (VARLEN) {
         // decode step: row r is query head hq + r, with its own scale
-        if (sc.one_token) qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq + min(SLICE ? (r & 31) : r, group - 1)) * nblk;
+        if (sc.step()) qi = (static_cast<int64_t>(w.sidx) * a.Hq + w.hq + min(SLICE ? (r & 31) : r, group - 1)) * nblk;
       }
       sq = __ldg(a.q_scale + qi);
       kv_scale_row = (static_cast<int64_t>(w.sidx) * a.Hkv + hkv) * nblk;
@@ -1098,7 +1101,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         const int jd = j - (w.c0 + qt);
         diag = jd >= 0;
         lim = w.dlt + r - 128 * jd;
-        if (sc.one_token) {          // every row is the token at position len - 1
+        if (sc.step()) {          // every row is the token at position len - 1
           const int ja = w.j0 + j;
           diag = (ja == ((w.len - 1) >> 7));
           lim = w.len - 1 - 128 * ja;
@@ -1236,7 +1239,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(w.row0 + q_row) * a.o_ss + w.hq * a.o_sh;
     bool store = q_row < w.len;
     if constexpr (VARLEN) {
-      if (sc.one_token) {            // row r: query head hq + r of the token
+      if (sc.step()) {            // row r: query head hq + r of the token
         orow = out + static_cast<int64_t>(w.row0) * a.o_ss + static_cast<int64_t>(w.hq + r) * a.o_sh;
         store = r < group;
       }
@@ -1260,7 +1263,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool DECODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
@@ -1272,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Sched<VARLEN> sc;
+  Sched<VARLEN, DECODE> sc;
   // The unit table comes by value (built on the host) or, when the sequence
   // offsets live on the device, from global memory (built by a kernel).
   sc.tab = tab_global ? tab_global : &tab;
@@ -1318,16 +1321,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE>(sm, &tm_q, &tm_k, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE, DECODE>(sm, &tm_q, &tm_k, a, sc, leader);
     } else if (warp == kLoadWarpV) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE>(sm, &tm_q, &tm_v, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE, DECODE>(sm, &tm_q, &tm_v, a, sc, leader);
     } else if (warp == kMmaWarp) {
       mma_role(sm, tmem, a, sc, leader);
     }
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE>(sm, tmem, a, sc, warp, lane);
+    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE, DECODE>(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -1338,12 +1341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false, bool DECODE = SLICE>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                    const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream,
                    const typename Sched<VARLEN>::Table* tab_global = nullptr) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE, DECODE>;
   // The shared-memory opt-in is per function and device: set it once.
   static bool opted_in[64] = {};
   int dev = 0;
@@ -1391,12 +1394,17 @@ long long table_units(const AttnArgs& a, const SeqTable& tab) {
 
 // Decode step with split key ranges: out = sum_s O_s 2^(m_s - M) /
 // sum_s l_s 2^(m_s - M), M = max_s m_s, for each (token, query head); one
-// block of 128 threads (one per output column) per (token, head).
+// block of 128 threads (one per output column) per (token, head). While the
+// device status word records a timed-out wait (the decode kernel stopped
+// before writing every partial row), out is left untouched.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __restrict__ part_o,
                                                              const float2* __restrict__ part_ml,
                                                              const __grid_constant__ CombineTable ct, int Hq,
                                                              __nv_bfloat16* __restrict__ out, int64_t o_ss,
-                                                             int64_t o_sh) {
+                                                             int64_t o_sh, const unsigned int* status) {
+  if (*reinterpret_cast<const volatile unsigned int*>(status) &
+      (kStatusLoaderTimeout | kStatusMmaTimeout | kStatusSoftmaxTimeout))
+    return;
   const int i = blockIdx.x / Hq, h = blockIdx.x - (blockIdx.x / Hq) * Hq;
   const int base = ct.base[i], cnt = ct.count[i];
   float mx = -INFINITY;
@@ -1412,11 +1420,15 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __rest
   out[static_cast<int64_t>(i) * o_ss + static_cast<int64_t>(h) * o_sh + threadIdx.x] = __float2bfloat16_rn(acc / den);
 }
 
+// Decode steps (a.one_token) run their own instantiations (DECODE), so the
+// packed and paged prefill kernels carry none of the one-token code.
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {
   const long long n = table_units(a, tab);
   if (a.replicate && a.Dqk == 128) return launch<128, false, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.replicate && a.Dqk == 192) return launch<192, false, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.one_token && a.Dqk == 128) return launch<128, false, true, false, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.one_token && a.Dqk == 192) return launch<192, false, true, false, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   return cudaErrorInvalidValue;
@@ -1427,6 +1439,8 @@ cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& t
   const long long n = table_units(a, tab);
   if (a.replicate && a.Dqk == 128) return launch<128, true, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.replicate && a.Dqk == 192) return launch<192, true, true, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.one_token && a.Dqk == 128) return launch<128, true, true, false, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
+  if (a.one_token && a.Dqk == 192) return launch<192, true, true, false, false, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128 && a.lean_p) return launch<128, true, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 128) return launch<128, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
   if (a.Dqk == 192) return launch<192, true, true>(tm_q, tm_k, tm_v, a, tab, n, stream);
@@ -1435,7 +1449,8 @@ cudaError_t launch_attn_fp8_varlen(const CUtensorMap& tm_q, const CUtensorMap& t
 
 cudaError_t launch_decode_combine(const AttnArgs& a, const CombineTable& ct, int N, cudaStream_t stream) {
   decode_combine_kernel<<<N * a.Hq, 128, 0, stream>>>(a.part_o, reinterpret_cast<const float2*>(a.part_ml), ct,
-                                                      a.Hq, static_cast<__nv_bfloat16*>(a.o), a.o_ss, a.o_sh);
+                                                      a.Hq, static_cast<__nv_bfloat16*>(a.o), a.o_ss, a.o_sh,
+                                                      a.status);
   return cudaGetLastError();
 }
 

@@ -378,7 +378,13 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  *              takes a quarter of every key block's columns; every split and
  *              copy writes its unnormalised rows with their offset and sum,
  *              and a second kernel combines them (results within rounding of
- *              the call without a workspace). NULL: neither.
+ *              the call without a workspace). NULL: neither. The workspace
+ *              bound counts the four copies only for Hq/Hkv <= 32. A split
+ *              is considered only while N*Hkv < 4 x the SM count, so a call
+ *              with Hq/Hkv > 32 and at least that many tasks runs as without
+ *              a workspace. If a wait of the decode kernel times out (status
+ *              bits 0-2, also while an earlier call's timeout is still
+ *              unread), the combine kernel leaves o untouched.
  *
  * q, o       : [N, Hq, Dqk|Dv]; q's token stride must be Hq x its head
  *              stride (each token's heads contiguous).

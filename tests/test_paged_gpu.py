@@ -256,18 +256,20 @@ def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, D, fp8):
     assert torch.equal(o, ref_gpu)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 8, 128), (64, 1, 128), (64, 1, 192)])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_decode_small_batch_long_context_splits(fp8):
-    """Two sequences of 9000 and 20000 positions, 8 KV heads: 16 tasks for
-    the whole GPU, so the key ranges are split into many pieces; against the
-    oracle, and within rounding of the unsplit call. Queries are scaled by 3
-    so the rows attend to a few hundred keys rather than near-uniformly to
-    all 20000 (a flat average of random values shrinks the output to the
-    size of the FP8 probability-rounding noise, split or not)."""
+def test_decode_small_batch_long_context_splits(Hq, Hkv, D, fp8):
+    """Two sequences of 9000 and 20000 positions: a handful of tasks for the
+    whole GPU, so the key ranges are split into many pieces; against the
+    oracle, and within rounding of the unsplit call. 16/8 heads replicate the
+    group's rows in the tile; 64 query heads per KV head (above 32) take the
+    split path with one copy of the rows. Queries are scaled by 3 so the rows
+    attend to a few hundred keys rather than near-uniformly to all 20000 (a
+    flat average of random values shrinks the output to the size of the FP8
+    probability-rounding noise, split or not)."""
     lens = [9000, 20000]
     seqs = [(L - 1, 1) for L in lens]
-    Hq, Hkv, D = 16, 8, 128
-    full = _sequences(seqs, Hq, Hkv, D, seed=41 + fp8)
+    full = _sequences(seqs, Hq, Hkv, D, seed=41 + fp8 + Hq + D)
     full = [((q.float() * 3).to(torch.bfloat16), k, v) for q, k, v in full]
     q, kc, vc, bt, cu = _paged(seqs, full)
     qd, kcd, vcd, btd = q.cuda(), kc.cuda(), vc.cuda(), bt.cuda()
@@ -290,7 +292,7 @@ def test_decode_small_batch_long_context_splits(fp8):
     ref = np.concatenate([oattn.causal_attention_prefix(qo[i:i + 1], _gather(ko, btn[i], L), _gather(vo, btn[i], L),
                                                         1 / math.sqrt(D)) for i, L in enumerate(lens)])
     gate = assert_fp8_gate if fp8 else assert_bf16_gate
-    gate(f32(o), ref, f"decode split fp8={fp8}")
+    gate(f32(o), ref, f"decode split fp8={fp8} Hq={Hq} Hkv={Hkv} D={D}")
     e_split = oattn.rel_l2(f32(o), ref)
     e_one = oattn.rel_l2(f32(o1), ref)
     assert e_split <= 1.25 * e_one + 1e-4, (e_split, e_one)
