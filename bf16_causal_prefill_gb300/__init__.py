@@ -64,13 +64,13 @@ def lib() -> ctypes.CDLL:
                                      vp, vp, vp, vp, vp]
     L.zyfa_attn_fwd_fp8.restype = c_int
     L.zyfa_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
-                                    c_float, vp, vp, vp, vp, vp]
+                                    c_float, vp, vp, vp, vp, c_int, vp]
     L.zyfa_attn_fwd_bf16_rows.restype = c_int
     L.zyfa_attn_fwd_bf16_rows.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                           vp, vp, vp, vp, c_int, c_int, vp]
     L.zyfa_attn_fwd_fp8_rows.restype = c_int
     L.zyfa_attn_fwd_fp8_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
-                                         c_float, vp, vp, vp, vp, c_int, c_int, vp]
+                                         c_float, vp, vp, vp, vp, c_int, c_int, c_int, vp]
     L.zyfa_quantize_fp8_rows.restype = c_int
     L.zyfa_quantize_fp8_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, c_int, c_int,
                                          c_int, c_int, c_int, c_int, c_int, vp]
@@ -78,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.zyfa_prefill_fp8_host_workspace.argtypes = [c_int] * 6
     L.zyfa_prefill_fp8_host.restype = c_int
     L.zyfa_prefill_fp8_host.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
-                                        c_int, vp, ctypes.c_size_t, vp]
+                                        c_int, vp, ctypes.c_size_t, c_int, vp]
     L.zyfa_varlen_workspace_bytes.restype = ctypes.c_size_t
     L.zyfa_varlen_workspace_bytes.argtypes = []
     L.zyfa_quantize_fp8_varlen_dev.restype = c_int
@@ -89,12 +89,12 @@ def lib() -> ctypes.CDLL:
                                                 c_float, vp, vp, vp, vp, vp, vp]
     L.zyfa_attn_fwd_fp8_varlen_dev.restype = c_int
     L.zyfa_attn_fwd_fp8_varlen_dev.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
-                                               c_int, c_int, c_float, vp, vp, vp, vp, vp, vp]
+                                               c_int, c_int, c_float, vp, vp, vp, vp, vp, c_int, vp]
     L.zyfa_noalloc_scratch_bytes.restype = ctypes.c_size_t
     L.zyfa_noalloc_scratch_bytes.argtypes = []
     L.zyfa_attn_fwd_fp8_varlen_dev_noalloc.restype = c_int
     L.zyfa_attn_fwd_fp8_varlen_dev_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
-                                                       c_int, c_int, c_int, c_float, vp, vp, vp, vp, vp]
+                                                       c_int, c_int, c_int, c_float, vp, vp, vp, vp, c_int, vp]
     L.zyfa_quantize_fp8_varlen.restype = c_int
     L.zyfa_quantize_fp8_varlen.argtypes = [vp, i64, i64, vp, vp, vp, c_int, c_int, c_int, c_int, vp]
     L.zyfa_attn_fwd_bf16_varlen.restype = c_int
@@ -102,13 +102,13 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, vp, vp, vp]
     L.zyfa_attn_fwd_fp8_varlen.restype = c_int
     L.zyfa_attn_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
-                                           c_float, vp, vp, vp, vp, vp]
+                                           c_float, vp, vp, vp, vp, c_int, vp]
     L.zyfa_attn_fwd_bf16_paged.restype = c_int
     L.zyfa_attn_fwd_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int, c_int, c_int,
                                            c_float, vp, vp, vp, vp, vp]
     L.zyfa_attn_fwd_fp8_paged.restype = c_int
     L.zyfa_attn_fwd_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
-                                          c_int, c_int, c_float, vp, vp, vp, vp, vp]
+                                          c_int, c_int, c_float, vp, vp, vp, vp, c_int, vp]
     L.zyfa_decode_workspace_bytes.restype = ctypes.c_size_t
     L.zyfa_decode_workspace_bytes.argtypes = [c_int, c_int, c_int]
     L.zyfa_attn_decode_bf16_paged.restype = c_int
@@ -116,11 +116,9 @@ def lib() -> ctypes.CDLL:
                                               c_float, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.zyfa_attn_decode_fp8_paged.restype = c_int
     L.zyfa_attn_decode_fp8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, c_int, c_int, c_int, c_int,
-                                             c_int, c_int, c_float, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+                                             c_int, c_int, c_float, vp, vp, vp, vp, vp, ctypes.c_size_t, c_int, vp]
     L.zyfa_get_device_status.restype = c_int
     L.zyfa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
-    L.zyfa_set_fp8_probabilities.restype = c_int
-    L.zyfa_set_fp8_probabilities.argtypes = [c_int]
     L.zyfa_set_debug.restype = c_int
     L.zyfa_set_debug.argtypes = [c_int, ctypes.c_double]
     _lib = L
@@ -212,7 +210,7 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
                  v8: torch.Tensor, v_scale: torch.Tensor, softmax_scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None,
-                 rows: Optional[Tuple[int, int]] = None) -> torch.Tensor:
+                 rows: Optional[Tuple[int, int]] = None, lean_p: bool = False) -> torch.Tensor:
     """Causal attention on per-block e4m3 inputs (uint8 codes + float32 block scales) -> bf16 o.
     rows=(begin, end): only those output rows (multiples of 256, or end = S)."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
@@ -234,18 +232,18 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
         _check(lib().zyfa_attn_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
                                        v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk, Dv,
                                        float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
-                                       _strides(out), _stream_ptr(q8, stream)))
+                                       _strides(out), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
     else:
         _check(lib().zyfa_attn_fwd_fp8_rows(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
                                             v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk,
                                             Dv, float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
-                                            _strides(out), int(rows[0]), int(rows[1]), _stream_ptr(q8, stream)))
+                                            _strides(out), int(rows[0]), int(rows[1]), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
     return out
 
 
 def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
                 softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None):
+                stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False):
     """The FP8 prefill path: quantise Q and K (optionally rotated) and V, then
     FP8 attention. Returns (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
@@ -253,7 +251,7 @@ def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: boo
     q8, qs = quantize_fp8(q, hadamard, stream=stream)
     k8, ks = quantize_fp8(k, hadamard, stream=stream)
     v8, vs = quantize_fp8(v, False, stream=stream)
-    o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream)
+    o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream, lean_p=lean_p)
     return o, (q8, qs, k8, ks, v8, vs)
 
 
@@ -269,7 +267,7 @@ def prefill_fp8_host_workspace(B: int, S: int, Hq: int, Hkv: int, Dqk: int, Dv: 
 def prefill_fp8_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
                      softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                      n_chunks: int = 0, workspace: Optional[torch.Tensor] = None,
-                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                     stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False) -> torch.Tensor:
     """The FP8 prefill on page-locked host tensors: copies in, quantisation,
     attention and the copy of O back run as one pipeline along the sequence.
     Returns the page-locked host o; it is valid once the stream (default: the
@@ -288,7 +286,7 @@ def prefill_fp8_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard
     s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
     _check(lib().zyfa_prefill_fp8_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
                                        Dqk, Dv, float(softmax_scale), int(bool(hadamard)), int(n_chunks),
-                                       workspace.data_ptr(), workspace.numel(), s.cuda_stream))
+                                       workspace.data_ptr(), workspace.numel(), _fp8_flags(lean_p), s.cuda_stream))
     return out
 
 
@@ -337,6 +335,11 @@ def _require_packed(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != 3 or t.stride(2) != 1:
         raise ValueError(f"{name} must be 3-D [T,H,D] with a contiguous last dim")
+
+
+def _fp8_flags(lean_p: bool) -> int:
+    """The flags word of the FP8 attention calls: lean P (head dim 128) or exact P."""
+    return 1 if lean_p else 0
 
 
 def _i64x2(a: int, b: int):
@@ -410,7 +413,7 @@ def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
                         v8: torch.Tensor, v_scale: torch.Tensor, cu_seqlens, softmax_scale: Optional[float] = None,
                         out: Optional[torch.Tensor] = None,
                         stream: Optional[torch.cuda.Stream] = None,
-                        max_seqlen: Optional[int] = None) -> torch.Tensor:
+                        max_seqlen: Optional[int] = None, lean_p: bool = False) -> torch.Tensor:
     """FP8 causal attention over a packed variable-length batch (codes and
     scales as written by quantize_fp8_varlen) -> bf16 o [T,Hq,Dv]. An int32
     CUDA cu_seqlens with max_seqlen given stays on the device."""
@@ -439,12 +442,12 @@ def attn_fwd_fp8_varlen(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
                                                   k_scale.data_ptr(), v8.data_ptr(), v_scale.data_ptr(),
                                                   out.data_ptr(), cu_ptr, B, T, max_len, Hq, Hkv, Dqk, Dv,
                                                   float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
-                                                  _strides2(out), ws.data_ptr(), _stream_ptr(q8, stream)))
+                                                  _strides2(out), ws.data_ptr(), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
         return out
     _check(lib().zyfa_attn_fwd_fp8_varlen(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
                                           v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, B, Hq, Hkv, Dqk,
                                           Dv, float(softmax_scale), _strides2(q8), _strides2(k8), _strides2(v8),
-                                          _strides2(out), _stream_ptr(q8, stream)))
+                                          _strides2(out), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
     return out
 
 
@@ -452,7 +455,7 @@ def attn_fwd_fp8_varlen_dev_noalloc(q8: torch.Tensor, q_scale: torch.Tensor, k8:
                                     k_scale: torch.Tensor, v8: torch.Tensor, v_scale: torch.Tensor,
                                     cu_seqlens: torch.Tensor, max_seqlen: int, out: torch.Tensor,
                                     softmax_scale: Optional[float] = None,
-                                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                                    stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False) -> torch.Tensor:
     """attn_fwd_fp8_varlen with device offsets for callers that cannot
     allocate device memory on the call path (a replayed CUDA graph with fixed
     memory, a serving loop drawing only from its own pool): the library keeps
@@ -480,13 +483,13 @@ def attn_fwd_fp8_varlen_dev_noalloc(q8: torch.Tensor, q_scale: torch.Tensor, k8:
                                                       k_scale.data_ptr(), v8.data_ptr(), v_scale.data_ptr(),
                                                       out.data_ptr(), cu_ptr, B, T, max_len, Hq, Hkv, Dqk, Dv,
                                                       float(softmax_scale), _strides2(q8), _strides2(k8),
-                                                      _strides2(v8), _strides2(out), _stream_ptr(q8, stream)))
+                                                      _strides2(v8), _strides2(out), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
     return out
 
 
 def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens, hadamard: bool = False,
                        softmax_scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None,
-                       max_seqlen: Optional[int] = None):
+                       max_seqlen: Optional[int] = None, lean_p: bool = False):
     """The FP8 prefill path over a packed variable-length batch. Returns
     (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
@@ -494,7 +497,8 @@ def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seq
     q8, qs = quantize_fp8_varlen(q, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
     k8, ks = quantize_fp8_varlen(k, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
     v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream, max_seqlen=max_seqlen)
-    o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream, max_seqlen=max_seqlen)
+    o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream, max_seqlen=max_seqlen,
+                            lean_p=lean_p)
     return o, (q8, qs, k8, ks, v8, vs)
 
 
@@ -563,7 +567,7 @@ def attn_fwd_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.
                        v_cache8: torch.Tensor, v_scale: torch.Tensor, cu_seqlens_q, ctx_lens,
                        block_table: torch.Tensor, softmax_scale: Optional[float] = None,
                        out: Optional[torch.Tensor] = None,
-                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                       stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False) -> torch.Tensor:
     """FP8 form of attn_fwd_bf16_paged: q8/q_scale from quantize_fp8_varlen on
     the packed queries, k/v caches and their [num_pages, Hkv] scales from
     quantize_fp8_cache. Returns o [T,Hq,Dv] bf16."""
@@ -588,7 +592,7 @@ def attn_fwd_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.
                                          v_cache8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), cu, ctx,
                                          block_table.data_ptr(), block_table.stride(0), P, B, Hq, Hkv, Dqk, Dv,
                                          float(softmax_scale), _strides2(q8), _strides(k_cache8), _strides(v_cache8),
-                                         _strides2(out), _stream_ptr(q8, stream)))
+                                         _strides2(out), _fp8_flags(lean_p), _stream_ptr(q8, stream)))
     return out
 
 
@@ -670,7 +674,8 @@ def attn_decode_bf16_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
 def attn_decode_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: torch.Tensor, k_scale: torch.Tensor,
                           v_cache8: torch.Tensor, v_scale: torch.Tensor, seq_lens, block_table: torch.Tensor,
                           softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                          stream: Optional[torch.cuda.Stream] = None, split=True) -> torch.Tensor:
+                          stream: Optional[torch.cuda.Stream] = None, split=True,
+                          lean_p: bool = False) -> torch.Tensor:
     """FP8 form of attn_decode_bf16_paged: q8/q_scale from quantize_fp8_decode,
     caches and their [num_pages, Hkv] scales from quantize_fp8_cache."""
     _require_packed(q8, "q8", torch.uint8)
@@ -694,7 +699,7 @@ def attn_decode_fp8_paged(q8: torch.Tensor, q_scale: torch.Tensor, k_cache8: tor
                                             k_scale.data_ptr(), v_cache8.data_ptr(), v_scale.data_ptr(),
                                             out.data_ptr(), lens, block_table.data_ptr(), block_table.stride(0), P,
                                             N, Hq, Hkv, Dqk, Dv, float(softmax_scale), _strides2(q8),
-                                            _strides(k_cache8), _strides(v_cache8), _strides2(out), ws_ptr, ws_bytes,
+                                            _strides(k_cache8), _strides(v_cache8), _strides2(out), ws_ptr, ws_bytes, _fp8_flags(lean_p),
                                             _stream_ptr(q8, stream)))
     return out
 
@@ -705,15 +710,6 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _check(lib().zyfa_get_device_status(s, ctypes.byref(w)))
     return w.value
-
-
-def set_fp8_probabilities(mode: str = "exact") -> None:
-    """FP8 attention probabilities: "exact" (default) or "lean" (head dim 128;
-    the e4m3 code approximated linearly, no exponential). Process-wide."""
-    modes = {"exact": 0, "lean": 1}
-    if mode not in modes:
-        raise ValueError(f"mode must be one of {sorted(modes)}")
-    _check(lib().zyfa_set_fp8_probabilities(modes[mode]))
 
 
 def set_debug(stall_loader: bool = False, timeout_seconds: float = 0.0) -> None:

@@ -30,6 +30,16 @@ int fail_cuda(cudaError_t e, const char* what) {
   return fail(ZYFA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// FP8 attention flags: ZYFA_FP8_LEAN_P selects lean P; no other bit is
+// defined. Returns 0 (exact P) or 1 (lean P), or -1 for unknown bits.
+int fp8_flags_lean(int flags) {
+  if (flags & ~ZYFA_FP8_LEAN_P) return -1;
+  return (flags & ZYFA_FP8_LEAN_P) ? 1 : 0;
+}
+int lean_flags_error(int flags) {
+  return fail(ZYFA_ERR_INVALID_ARG, "unknown FP8 flags 0x%x (only ZYFA_FP8_LEAN_P is defined)", flags);
+}
+
 // Per-device state, filled on first use of a device.
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -42,7 +52,6 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
 uint64_t g_timeout_ns = 2000000000ull;
-int g_lean_p = 0;   // FP8 probabilities: 0 exact, 1 lean (head dim 128)
 int g_debug_stall = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -198,12 +207,6 @@ int zyfa_set_debug(int stall_loader, double timeout_seconds) {
   return ZYFA_OK;
 }
 
-int zyfa_set_fp8_probabilities(int mode) {
-  if (mode != 0 && mode != 1) return fail(ZYFA_ERR_INVALID_ARG, "mode must be 0 (exact) or 1 (lean)");
-  g_lean_p = mode;
-  return ZYFA_OK;
-}
-
 static int quant_common(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
                         float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
                         void* stream) {
@@ -278,7 +281,7 @@ int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, in
                       stream);
 }
 
-static int attn_common(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
+static int attn_common(bool fp8, int lean, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[3], const int64_t ks[3], const int64_t vs[3],
                        const int64_t os[3], int row_begin, int row_end, void* stream) {
@@ -313,7 +316,7 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = (S + 127) / 128;
-  a.lean_p = g_lean_p;
+  a.lean_p = lean;
   a.pair_lo = row_begin / 256;
   a.pair_hi = (row_end + 255) / 256;
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
@@ -325,15 +328,17 @@ static int attn_common(bool fp8, const void* q, const float* qsc, const void* k,
 int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                        int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                        const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
-  return attn_common(false, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
+  return attn_common(false, 0, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
                      k_strides, v_strides, o_strides, 0, S, stream);
 }
 
 int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale, const void* v8,
                       const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
                       float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
-                      const int64_t v_strides[3], const int64_t o_strides[3], void* stream) {
-  return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
+                      const int64_t v_strides[3], const int64_t o_strides[3], int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_common(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, 0, S, stream);
 }
 
@@ -341,7 +346,7 @@ int zyfa_attn_fwd_bf16_rows(const void* q, const void* k, const void* v, void* o
                             int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
                             const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
                             int row_begin, int row_end, void* stream) {
-  return attn_common(false, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
+  return attn_common(false, 0, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
                      k_strides, v_strides, o_strides, row_begin, row_end, stream);
 }
 
@@ -349,8 +354,10 @@ int zyfa_attn_fwd_fp8_rows(const void* q8, const float* q_scale, const void* k8,
                            const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                            int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                            const int64_t v_strides[3], const int64_t o_strides[3], int row_begin, int row_end,
-                           void* stream) {
-  return attn_common(true, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
+                           int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_common(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, row_begin, row_end, stream);
 }
 
@@ -424,7 +431,7 @@ static void build_seq_table(const int32_t* cu, const int32_t* ctx, int B, int ma
     tab->level_start[kl + 1] = tab->level_start[kl] + cnt[tab->n_levels - 1 - kl] * Hq;
 }
 
-static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
+static int attn_varlen(bool fp8, int lean, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, const int32_t* cu, int B, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[2], const int64_t ks[2], const int64_t vs[2],
                        const int64_t os[2], void* stream, const int32_t* cu_dev = nullptr, int total_dev = 0,
@@ -468,7 +475,7 @@ static int attn_varlen(bool fp8, const void* q, const float* qsc, const void* k,
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = (max_len + 127) / 128;
-  a.lean_p = g_lean_p;
+  a.lean_p = lean;
   if (cu_dev) {
     auto* dtab = static_cast<zyfa::SeqTable*>(workspace);
     cudaError_t e = zyfa::launch_build_seq_tables(cu_dev, B, T, max_len, Hq, dtab, nullptr, d->status,
@@ -491,7 +498,7 @@ int zyfa_attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, void*
                               int Hq, int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                               const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
                               void* stream) {
-  return attn_varlen(false, q, nullptr, k, nullptr, v, nullptr, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+  return attn_varlen(false, 0, q, nullptr, k, nullptr, v, nullptr, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream);
 }
 
@@ -499,13 +506,15 @@ int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k
                              const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens, int B, int Hq,
                              int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                              const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
-                             void* stream) {
-  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                             int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_varlen(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, cu_seqlens, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream);
 }
 
 // Packed queries over a paged K/V cache (chunked prefill, prefix caching).
-static int attn_paged(bool fp8, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
+static int attn_paged(bool fp8, int lean, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
                       const float* vsc, void* o, const int32_t* cu, const int32_t* ctx_lens,
                       const int32_t* block_table, int64_t bt_stride, int num_pages, int B, int Hq, int Hkv, int Dqk,
                       int Dv, float softmax_scale, const int64_t qs[2], const int64_t kcs[3], const int64_t vcs[3],
@@ -558,7 +567,7 @@ static int attn_paged(bool fp8, const void* q, const float* qsc, const void* kc,
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = (max_len + 127) / 128;
-  a.lean_p = g_lean_p;
+  a.lean_p = lean;
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.num_pages = num_pages;
@@ -575,7 +584,7 @@ int zyfa_attn_fwd_bf16_paged(const void* q, const void* k_cache, const void* v_c
                              int64_t block_table_stride, int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv,
                              float softmax_scale, const int64_t q_strides[2], const int64_t k_cache_strides[3],
                              const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
-  return attn_paged(false, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, cu_seqlens_q, ctx_lens, block_table,
+  return attn_paged(false, 0, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, cu_seqlens_q, ctx_lens, block_table,
                     block_table_stride, num_pages, B, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
                     v_cache_strides, o_strides, stream);
 }
@@ -585,8 +594,10 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
                             const int32_t* ctx_lens, const int32_t* block_table, int64_t block_table_stride,
                             int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                             const int64_t q_strides[2], const int64_t k_cache_strides[3],
-                            const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream) {
-  return attn_paged(true, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, cu_seqlens_q, ctx_lens, block_table,
+                            const int64_t v_cache_strides[3], const int64_t o_strides[2], int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_paged(true, lean, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, cu_seqlens_q, ctx_lens, block_table,
                     block_table_stride, num_pages, B, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
                     v_cache_strides, o_strides, stream);
 }
@@ -616,7 +627,7 @@ static size_t decode_ws_bytes(int N, int Hq, int Hkv) {
 }
 
 // Decode step over a paged cache: one query token per sequence.
-static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
+static int attn_decode(bool fp8, int lean, const void* q, const float* qsc, const void* kc, const float* ksc, const void* vc,
                        const float* vsc, void* o, const int32_t* seq_lens, const int32_t* block_table,
                        int64_t bt_stride, int num_pages, int N, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                        const int64_t qs[2], const int64_t kcs[3], const int64_t vcs[3], const int64_t os[2],
@@ -676,7 +687,7 @@ static int attn_decode(bool fp8, const void* q, const float* qsc, const void* kc
   a.debug_stall = g_debug_stall;
   a.num_sms = d->sm_count;
   a.scale_blocks = 1;          // q_scale [N, Hq]: one per token and head
-  a.lean_p = g_lean_p;
+  a.lean_p = lean;
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.num_pages = num_pages;
@@ -776,7 +787,7 @@ int zyfa_attn_decode_bf16_paged(const void* q, const void* k_cache, const void* 
                                 const int64_t q_strides[2], const int64_t k_cache_strides[3],
                                 const int64_t v_cache_strides[3], const int64_t o_strides[2], void* workspace,
                                 size_t workspace_bytes, void* stream) {
-  return attn_decode(false, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, seq_lens, block_table,
+  return attn_decode(false, 0, q, nullptr, k_cache, nullptr, v_cache, nullptr, o, seq_lens, block_table,
                      block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
                      v_cache_strides, o_strides, workspace, workspace_bytes, stream);
 }
@@ -786,8 +797,10 @@ int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void*
                                const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
                                int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                                const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
-                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_decode(true, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, seq_lens, block_table,
+                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_decode(true, lean, q8, q_scale, k_cache8, k_scale, v_cache8, v_scale, o, seq_lens, block_table,
                      block_table_stride, num_pages, N, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides, k_cache_strides,
                      v_cache_strides, o_strides, workspace, workspace_bytes, stream);
 }
@@ -884,7 +897,7 @@ int zyfa_attn_fwd_bf16_varlen_dev(const void* q, const void* k, const void* v, v
                                   float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
                                   const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
                                   void* stream) {
-  return attn_varlen(false, q, nullptr, k, nullptr, v, nullptr, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+  return attn_varlen(false, 0, q, nullptr, k, nullptr, v, nullptr, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
                      workspace);
 }
@@ -894,8 +907,10 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
                                  int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
                                  float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
                                  const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
-                                 void* stream) {
-  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+                                 int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_varlen(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
                      workspace);
 }
@@ -946,7 +961,9 @@ int zyfa_attn_fwd_fp8_varlen_dev_noalloc(const void* q8, const float* q_scale, c
                                          const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen,
                                          int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                                          const int64_t q_strides[2], const int64_t k_strides[2],
-                                         const int64_t v_strides[2], const int64_t o_strides[2], void* stream) {
+                                         const int64_t v_strides[2], const int64_t o_strides[2], int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
   // The static table bounds the batch: refuse what it cannot hold before
   // touching the device.
   if (B < 1 || B > zyfa::kMaxVarlenSeqs)
@@ -957,7 +974,7 @@ int zyfa_attn_fwd_fp8_varlen_dev_noalloc(const void* q8, const float* q_scale, c
                 max_seqlen, 2 * 128 * zyfa::kMaxVarlenLevels);
   void* scratch = nullptr;
   if (int r = noalloc_scratch(&scratch)) return r;
-  return attn_varlen(true, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
+  return attn_varlen(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, nullptr, B, Hq, Hkv, Dqk, Dv, softmax_scale,
                      q_strides, k_strides, v_strides, o_strides, stream, cu_seqlens_dev, total_tokens, max_seqlen,
                      scratch);
 }
@@ -1048,7 +1065,9 @@ size_t zyfa_prefill_fp8_host_workspace(int B, int S, int Hq, int Hkv, int Dqk, i
 
 int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
                           int Dqk, int Dv, float softmax_scale, int hadamard, int n_chunks, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+                          size_t workspace_bytes, int flags, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
   if (!q || !k || !v || !o || !workspace) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1)
     return fail(ZYFA_ERR_INVALID_ARG, "B, S, Hq, Hkv must be >= 1 (got %d, %d, %d, %d)", B, S, Hq, Hkv);
@@ -1125,7 +1144,7 @@ int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, 
       rc = fail_cuda(e, "host pipeline: order attention");
       break;
     }
-    if ((rc = attn_common(true, q8, qs, k8, ks, v8, vs, od, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, sq, sk, sv, so,
+    if ((rc = attn_common(true, lean, q8, qs, k8, ks, v8, vs, od, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, sq, sk, sv, so,
                           r0, r1, sa)))
       break;
     if ((e = cudaEventRecord(p->done[c], sa)) != cudaSuccess || (e = cudaStreamWaitEvent(p->d2h, p->done[c], 0)) != cudaSuccess ||

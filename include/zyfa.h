@@ -146,12 +146,24 @@ int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int
  * q8/k8/v8 : uint8 e4m3 [B,S,H,D] with the given strides (multiples of 16
  *            elements), 16-byte aligned.
  * q_scale  : float [B,Hq,ceil(S/128)], k_scale/v_scale: float [B,Hkv,ceil(S/128)].
+ * flags    : how this call computes the rounded probabilities (every FP8
+ *            attention call takes this argument; it affects that call only):
+ *            0 (ZYFA_FP8_EXACT_P): 2^x by the exponential unit, then RNE to
+ *            e4m3; ZYFA_FP8_LEAN_P ("ZYFA ...", "Lean P: Linear
+ *            Approximation of the FP8 Code"): the e4m3 code of 2^x taken as
+ *            round(8x + 56), no exponential, at head dim 128 (at 192, the
+ *            MLA shape, and in decode steps exact P is used, as the pages
+ *            keep it there); faster, with a larger probability-rounding
+ *            error (the normalisation by the rounded row sum still holds
+ *            exactly). Any other bit: ZYFA_ERR_INVALID_ARG.
  * Other arguments and errors as zyfa_attn_fwd_bf16.
  */
+#define ZYFA_FP8_EXACT_P 0
+#define ZYFA_FP8_LEAN_P 1
 int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
                       const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                       int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
-                      const int64_t v_strides[3], const int64_t o_strides[3], void* stream);
+                      const int64_t v_strides[3], const int64_t o_strides[3], int flags, void* stream);
 
 /*
  * Row-range ("chunked prefill") forms of the two calls above: only output rows
@@ -171,7 +183,7 @@ int zyfa_attn_fwd_fp8_rows(const void* q8, const float* q_scale, const void* k8,
                            const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                            int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                            const int64_t v_strides[3], const int64_t o_strides[3], int row_begin, int row_end,
-                           void* stream);
+                           int flags, void* stream);
 
 /*
  * The FP8 prefill from host memory: Q, K, V go to the device, are quantised
@@ -199,7 +211,7 @@ int zyfa_attn_fwd_fp8_rows(const void* q8, const float* q_scale, const void* k8,
 size_t zyfa_prefill_fp8_host_workspace(int B, int S, int Hq, int Hkv, int Dqk, int Dv);
 int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
                           int Dqk, int Dv, float softmax_scale, int hadamard, int n_chunks, void* workspace,
-                          size_t workspace_bytes, void* stream);
+                          size_t workspace_bytes, int flags, void* stream);
 
 /*
  * Packed variable-length batches. The pages time equal-length batches and
@@ -229,7 +241,7 @@ int zyfa_attn_fwd_fp8_varlen(const void* q8, const float* q_scale, const void* k
                              const void* v8, const float* v_scale, void* o, const int32_t* cu_seqlens, int B, int Hq,
                              int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                              const int64_t k_strides[2], const int64_t v_strides[2], const int64_t o_strides[2],
-                             void* stream);
+                             int flags, void* stream);
 
 /*
  * zyfa_quantize_fp8 for a packed variable-length tensor x [T,H,D] (same
@@ -276,7 +288,7 @@ int zyfa_attn_fwd_fp8_varlen_dev(const void* q8, const float* q_scale, const voi
                                  int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
                                  float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
                                  const int64_t v_strides[2], const int64_t o_strides[2], void* workspace,
-                                 void* stream);
+                                 int flags, void* stream);
 
 /*
  * zyfa_attn_fwd_fp8_varlen_dev without a workspace: an addition of this
@@ -309,7 +321,8 @@ int zyfa_attn_fwd_fp8_varlen_dev_noalloc(const void* q8, const float* q_scale, c
                                          const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen,
                                          int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                                          const int64_t q_strides[2], const int64_t k_strides[2],
-                                         const int64_t v_strides[2], const int64_t o_strides[2], void* stream);
+                                         const int64_t v_strides[2], const int64_t o_strides[2], int flags,
+                                         void* stream);
 
 /*
  * Packed queries over a PAGED K/V cache: chunked prefill and prefix caching.
@@ -356,7 +369,8 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
                             const int32_t* ctx_lens, const int32_t* block_table, int64_t block_table_stride,
                             int num_pages, int B, int Hq, int Hkv, int Dqk, int Dv, float softmax_scale,
                             const int64_t q_strides[2], const int64_t k_cache_strides[3],
-                            const int64_t v_cache_strides[3], const int64_t o_strides[2], void* stream);
+                            const int64_t v_cache_strides[3], const int64_t o_strides[2], int flags,
+                            void* stream);
 
 /*
  * Decode step over a paged K/V cache: one new token per sequence (its keys
@@ -407,7 +421,8 @@ int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void*
                                const int32_t* block_table, int64_t block_table_stride, int num_pages, int N, int Hq,
                                int Hkv, int Dqk, int Dv, float softmax_scale, const int64_t q_strides[2],
                                const int64_t k_cache_strides[3], const int64_t v_cache_strides[3],
-                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, void* stream);
+                               const int64_t o_strides[2], void* workspace, size_t workspace_bytes, int flags,
+                               void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -421,19 +436,6 @@ int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void*
  * `word` may be NULL.
  */
 int zyfa_get_device_status(void* stream, unsigned int* word);
-
-/*
- * How the FP8 attention calls compute the rounded probabilities (process-wide,
- * not thread-safe; applies to calls enqueued afterwards):
- *   0: exact P (default): 2^x by the exponential unit, then RNE to e4m3;
- *   1: lean P ("ZYFA ...", "Lean P: Linear Approximation of the FP8 Code"):
- *      the e4m3 code of 2^x approximated by round(8x + 56), no exponential;
- *      head dim 128 only (the MLA shape keeps exact P, as on the pages).
- *      Faster, with a larger probability-rounding error (the normalisation
- *      by the rounded row sum still holds exactly).
- * Returns ZYFA_ERR_INVALID_ARG for another mode.
- */
-int zyfa_set_fp8_probabilities(int mode);
 
 /*
  * Test hooks (process-wide, not thread-safe). stall_loader != 0 makes the

@@ -81,8 +81,18 @@ def test_quantiser_rejects_bad_arguments_on_host(L):
 
 def test_fp8_attention_needs_scales(L):
     rc = L.zyfa_attn_fwd_fp8(16, None, 16, 16, 16, 16, 16, 1, 128, 2, 1, 128, 128, ctypes.c_float(0.1),
-                             I3(256, 256, 128), I3(128, 128, 128), I3(128, 128, 128), I3(256, 256, 128), None)
+                             I3(256, 256, 128), I3(128, 128, 128), I3(128, 128, 128), I3(256, 256, 128), 0, None)
     assert rc == 1
+
+
+@pytest.mark.parametrize("flags", [2, 4, -1, 0x100])
+def test_fp8_attention_refuses_unknown_flags(L, flags):
+    # the flags word selects exact or lean probabilities per call; other bits are refused
+    rc = L.zyfa_attn_fwd_fp8(16, 16, 16, 16, 16, 16, 16, 1, 128, 2, 1, 128, 128, ctypes.c_float(0.1),
+                             I3(256, 256, 128), I3(128, 128, 128), I3(128, 128, 128), I3(256, 256, 128), flags,
+                             None)
+    assert rc == 1
+    assert b"flags" in L.zyfa_last_error_message()
 
 
 def test_python_binding_refuses_cpu_tensors():
@@ -140,7 +150,7 @@ def _rows(L, fp8, r0, r1, S=1000):
     st = (I3(S * 256, 256, 128), I3(S * 128, 128, 128), I3(S * 128, 128, 128), I3(S * 256, 256, 128))
     if fp8:
         return L.zyfa_attn_fwd_fp8_rows(16, 16, 16, 16, 16, 16, 16, 1, S, 2, 1, 128, 128, ctypes.c_float(0.1),
-                                        *st, r0, r1, None)
+                                        *st, r0, r1, 0, None)
     return L.zyfa_attn_fwd_bf16_rows(16, 16, 16, 16, 1, S, 2, 1, 128, 128, ctypes.c_float(0.1), *st, r0, r1, None)
 
 
@@ -178,7 +188,7 @@ def test_host_prefill_rejects_bad_arguments_on_host(L):
     def call(**kw):
         a = dict(ok, **kw)
         return p(a["q"], a["k"], a["v"], a["o"], 1, 512, a["Hq"], a["Hkv"], a["Dqk"], a["Dv"],
-                 ctypes.c_float(a["scale"]), a["had"], a["chunks"], a["ws"], a["wsn"], None)
+                 ctypes.c_float(a["scale"]), a["had"], a["chunks"], a["ws"], a["wsn"], 0, None)
 
     assert call(q=0) == 1                     # null pointer
     assert call(ws=0) == 1                    # no workspace
@@ -308,7 +318,7 @@ def test_noalloc_call_refuses_what_its_static_table_cannot_hold(L):
     s2 = (ctypes.c_int64 * 2)(128, 128)
     def call(B, max_len):
         return L.zyfa_attn_fwd_fp8_varlen_dev_noalloc(16, 16, 16, 16, 16, 16, 16, 16, B, 1000, max_len, 1, 1, 128,
-                                                       128, ctypes.c_float(0.1), s2, s2, s2, s2, None)
+                                                       128, ctypes.c_float(0.1), s2, s2, s2, s2, 0, None)
     assert call(2000, 1000) == 1
     assert b"static scratch" in L.zyfa_last_error_message()
     assert call(0, 1000) == 1

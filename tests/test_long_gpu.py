@@ -42,12 +42,8 @@ def test_bf16_128k(inputs):
 @pytest.mark.parametrize("mode", ["exact", "lean"])
 def test_fp8_128k(inputs, mode):
     q, k, v = inputs
-    zyfa.set_fp8_probabilities(mode)
-    try:
-        o, _ = zyfa.prefill_fp8(q.cuda(), k.cuda(), v.cuda())
-        zyfa.device_status()
-    finally:
-        zyfa.set_fp8_probabilities("exact")
+    o, _ = zyfa.prefill_fp8(q.cuda(), k.cuda(), v.cuda(), lean_p=(mode == "lean"))
+    zyfa.device_status()
     kdq = oracle_dequant(*oracle_quant(k, False))
     vdq = oracle_dequant(*oracle_quant(v, False))
     qdq = np.zeros(q.shape, np.float32)
