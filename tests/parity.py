@@ -4,6 +4,7 @@ oracle never sees a value produced by the CUDA path."""
 from __future__ import annotations
 
 import math
+import os
 from typing import Dict, List, Optional
 
 import numpy as np
@@ -109,3 +110,23 @@ def fp8_quant_blocks_for_rows(x: torch.Tensor, rows: List[int], hadamard: bool):
         sl = x[:, j * 128:(j + 1) * 128]
         res[j] = oracle_quant(sl, hadamard)
     return res
+
+
+def full_oracle(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, workers: int = 8) -> np.ndarray:
+    """The oracle's full output [B,S,Hq,Dv] (float64), one (batch, head) per
+    task over a pool of spawned processes (safe after CUDA is initialised)."""
+    import multiprocessing as mp
+    import oracle_pool
+    B, S, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    group = Hq // Hkv
+    tasks = [(np.asarray(q[b, :, h], np.float64), np.asarray(k[b, :, h // group], np.float64),
+              np.asarray(v[b, :, h // group], np.float64), scale) for b in range(B) for h in range(Hq)]
+    n = max(1, min(workers, os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(n) as pool:
+        outs = pool.map(oracle_pool.head_output, tasks, chunksize=1)
+    out = np.empty((B, S, Hq, v.shape[3]))
+    for i, o in enumerate(outs):
+        out[i // Hq, :, i % Hq] = o
+    return out
+

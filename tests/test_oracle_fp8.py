@@ -238,3 +238,59 @@ def test_mutant_wrong_max_is_caught():
     deq = fp8.e4m3_decode(fp8.e4m3_rne(q)) * np.float64(bad_scale)
     bound = np.maximum(np.abs(x) * 2.0 ** -4, bad_scale * 2.0 ** -10) * (1 + 1e-6)
     assert np.any(np.abs(deq - x) > bound)
+
+
+# ------------------------------------------------- division, pinned exactly --
+# Reading: the quantiser divides, code = RNE_e4m3(fl32(y / s)) with an IEEE
+# float32 division ("FP8 GEMM on CDNA4", 2.2: scale = amax / max, values
+# divided by the scale). The cases below (bf16 y, bf16 amax) are ones where
+# multiplying by the rounded reciprocal, fl32(y * fl32(1 / s)), gives another
+# code: y / s lands exactly on an e4m3 rounding midpoint, which the division
+# keeps (and the tie goes to the even code) while the reciprocal moves it to
+# one side. Expected codes come from exact rational arithmetic only.
+from fractions import Fraction
+
+DIVISION_CASES = [(1.2734375, 1.9431114196777344e-05), (2.84375, 8.058547973632812e-05),
+                  (3.0625, 0.00016689300537109375)]
+
+
+def _rn_f32(x: Fraction) -> Fraction:
+    """x > 0 rounded to the nearest float32 (ties to an even significand), exactly."""
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    if Fraction(2) ** e > x:
+        e -= 1
+    ulp = Fraction(2) ** (max(e, -126) - 23)
+    n, r = divmod(x, ulp)
+    n = int(n)
+    if r > ulp / 2 or (r == ulp / 2 and n % 2 == 1):
+        n += 1
+    return n * ulp
+
+
+def _e4m3_exact(x: Fraction) -> int:
+    """Code of the e4m3 value nearest to x >= 0 (ties to the even code), by
+    search over the 127 non-negative finite codes, saturating at 448."""
+    best, best_d = 0, None
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        v = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        d = abs(v - x)
+        if best_d is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best
+
+
+@pytest.mark.parametrize("amax,y", DIVISION_CASES)
+def test_quantiser_divides_in_float32(amax, y):
+    s_exact = _rn_f32(Fraction(amax) / 448)
+    want = _e4m3_exact(_rn_f32(Fraction(y) / s_exact))
+    via_reciprocal = _e4m3_exact(_rn_f32(Fraction(y) * _rn_f32(1 / s_exact)))
+    assert want != via_reciprocal                       # the case tells the two readings apart
+    x = np.zeros((1, 128, 1, 128), np.float32)
+    x[0, 0, 0, 0] = amax                                # fixes the block's scale
+    x[0, 1, 0, 0] = y
+    x[0, 2, 0, 0] = -y
+    codes, scales = fp8.quantize_fp8(x)
+    assert Fraction(float(scales[0, 0, 0])) == s_exact
+    assert int(codes[0, 1, 0, 0]) == want
+    assert int(codes[0, 2, 0, 0]) == 0x80 | want        # sign bit over the same magnitude

@@ -4,7 +4,9 @@ heads, a set of rows per head that includes row 0, tile edges and the last
 row. The FP8 path is checked end to end: the GPU quantiser's codes for K, V
 and the sampled Q blocks must equal the oracle's bit for bit, and the output
 rows must meet the FP8 gate against the oracle on the oracle's dequantised
-inputs. The error against unquantised fp64 attention is printed."""
+inputs. The error against unquantised fp64 attention is printed. The batch-2
+8K workload is also checked in full (every output element, BF16 and FP8), the
+oracle spread over a pool of processes."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +14,7 @@ import torch
 import bf16_causal_prefill_gb300 as zyfa
 import workloads
 from oracle import attention as oattn
-from parity import (assert_bf16_gate, assert_fp8_gate, f32, fp8_quant_blocks_for_rows, gpu_rows,
+from parity import (assert_bf16_gate, assert_fp8_gate, f32, fp8_quant_blocks_for_rows, full_oracle, gpu_rows,
                     oracle_dequant, oracle_quant, sampled_rows_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -86,3 +88,31 @@ def test_fp8_sampled_rows(name, hadamard):
     ref_exact = sampled_rows_oracle(f32(q), f32(k), f32(v), w.softmax_scale, rows)
     print(f"\n{name} fp8 hadamard={had}: vs dequantised oracle {e}, "
           f"vs unquantised fp64 rel_l2={oattn.rel_l2(got, ref_exact):.3e}")
+
+
+FULL = "gauss_b2_gqa32x8_s8k_d128"
+
+
+@pytest.mark.parametrize("path", ["bf16", "fp8"])
+def test_full_output_b2_8k(path):
+    w, q, k, v = _load(FULL)
+    if path == "bf16":
+        o = zyfa.attn_fwd_bf16(q.cuda(), k.cuda(), v.cuda(), w.softmax_scale)
+        zyfa.device_status()
+        qo, ko, vo = f32(q), f32(k), f32(v)
+    else:
+        o, (q8, qs, k8, ks, v8, vs) = zyfa.prefill_fp8(q.cuda(), k.cuda(), v.cuda())
+        zyfa.device_status()
+        deq = []
+        for x, c8, sc in ((q, q8, qs), (k, k8, ks), (v, v8, vs)):
+            c, s = oracle_quant(x, False)
+            assert np.array_equal(c8.cpu().numpy(), c) and np.array_equal(sc.cpu().numpy(), s)
+            deq.append(oracle_dequant(c, s))
+        qo, ko, vo = deq
+    got = f32(o)
+    del o
+    ref = full_oracle(qo, ko, vo, w.softmax_scale)
+    gate = assert_bf16_gate if path == "bf16" else assert_fp8_gate
+    e = gate(got, ref, f"{path} {FULL} full output")
+    print(f"\n{FULL} {path} full output: {e}")
+
