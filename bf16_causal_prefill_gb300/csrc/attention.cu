@@ -133,27 +133,27 @@ struct Unit {
   int sidx;                // sequence index of the scale arrays
 };
 
-// Work order. The (batch, KV head) groups are taken kGroupsInFlight at a
-// time; inside such a super-group the longest query-tile pairs come first and,
-// for each pair, the groups and then their query heads are adjacent. Units in
-// flight then share a few KV heads (K/V stay in L2) without every CTA
-// streaming the very same K/V tile at once.
-constexpr int kGroupsInFlight = 8;
+// Work order. The (batch, KV head) groups are taken `gif` at a time (the
+// host picks gif, AttnArgs::groups_in_flight); inside such a super-group the
+// longest query-tile pairs come first and, for each pair, the groups and then
+// their query heads are adjacent. Units in flight then share a few KV heads
+// (K/V stay in L2) without every CTA streaming the very same K/V tile at once.
 
 // Pairs pair_lo .. pair_hi - 1 only (a row range of a chunked prefill).
-__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles, int pair_lo, int pair_hi) {
+__device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n_qtiles, int pair_lo, int pair_hi,
+                                            int gif) {
   const int n_pairs = pair_hi - pair_lo;
   const int G = Hq / Hkv;
   const int n_groups = B * Hkv;
-  const int per_sg = kGroupsInFlight * G * n_pairs;
+  const int per_sg = gif * G * n_pairs;
   const int sg = u / per_sg;
   const int r = u - sg * per_sg;
-  const int gs_here = min(kGroupsInFlight, n_groups - sg * kGroupsInFlight);
+  const int gs_here = min(gif, n_groups - sg * gif);
   const int per_t = gs_here * G;
   const int tq = r / per_t;
   const int rr = r - tq * per_t;
   const int gi = rr / G;
-  const int group = sg * kGroupsInFlight + gi;
+  const int group = sg * gif + gi;
   Unit w;
   w.b = group / Hkv;
   const int hkv = group - w.b * Hkv;
@@ -183,6 +183,7 @@ struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
+  int groups_in_flight;    // equal lengths: KV groups per super-group of the work order
   bool one_token;          // decode step: one query token per sequence, its heads as tile rows (DECODE only)
   __device__ __forceinline__ bool step() const { return DECODE && one_token; }
   int split_tiles;         // decode step: nonzero when key ranges are split (per-sequence split counts in tab)
@@ -278,7 +279,7 @@ struct Sched {
       w.n_kv = w.has_b ? w.n_b : w.n_a;
       return w;
     } else {
-      Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles, pair_lo, pair_hi);
+      Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles, pair_lo, pair_hi, groups_in_flight);
       w.len = S;
       return w;
     }
@@ -1286,6 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.n_qtiles = (a.S + 127) / 128;
   sc.pair_lo = a.pair_lo;
   sc.pair_hi = a.pair_hi;
+  sc.groups_in_flight = max(1, a.groups_in_flight);
   sc.one_token = a.one_token != 0;
   sc.split_tiles = a.split_tiles;
 

@@ -78,6 +78,7 @@ struct AttnArgs {
   int scale_blocks;        // fp8: blocks per (sequence, head) row of the scale arrays
   int lean_p;              // fp8, head dim 128: lean P instead of exact P
   int pair_lo, pair_hi;    // equal lengths: only query-tile pairs [pair_lo, pair_hi) (rows 256*lo .. 256*hi)
+  int groups_in_flight;    // equal lengths: (batch, KV head) groups interleaved in the work order
   // Paged K/V (packed queries only): key block j of sequence i (caller's
   // order) is page block_table[i * bt_stride + j] of caches viewed as
   // [num_pages, 128, Hkv, D]; fp8 K/V scales are [num_pages, Hkv]. Null: K/V
