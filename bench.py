@@ -42,6 +42,11 @@ METRIC = "causal prefill attn TFLOP/s (FP8, BF16) at 32K tokens; % of GB300 dens
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor-core rate ratio on GB300
+# Per-SM issue rates of the softmax's two special-function steps, measured on
+# a GB300 with a register-only microbenchmark (4 warps per sub-partition):
+# ex2.approx.ftz.f32 results and cvt.rn.satfinite.e4m3x2.f32 elements per clock.
+EX2_PER_CLK_SM = 32.0
+E4M3_CVT_PER_CLK_SM = 69.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -79,12 +84,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_from_profiles(kernel_file: str, tag: str):
-    """Per-launch DRAM bytes recorded in profiles/ for `tag`, if the kernel
-    source still has the hash the counters were taken with; else None."""
-    src = os.path.join(ROOT, "bf16_causal_prefill_gb300", "csrc", kernel_file)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+# The attention kernel and the host code that picks its work order (the
+# order decides how much K/V is re-read from HBM).
+ATTN_SOURCES = ("attention.cu", "api.cu")
+
+
+def source_hash(*kernel_files: str) -> str:
+    """First 16 hex digits of the SHA-256 of the named csrc files, concatenated."""
+    hs = hashlib.sha256()
+    for kernel_file in kernel_files:
+        with open(os.path.join(ROOT, "bf16_causal_prefill_gb300", "csrc", kernel_file), "rb") as f:
+            hs.update(f.read())
+    return hs.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_files, tag: str):
+    """Per-launch DRAM bytes recorded in profiles/ for `tag`, if the sources
+    still have the hash the counters were taken with; else None."""
+    h = source_hash(*kernel_files)
     pat = re.compile(rf"^traffic\[{re.escape(tag)}\]:\s*([0-9.eE+]+)\s+bytes/launch\s+src=([0-9a-f]+)")
     pdir = os.path.join(ROOT, "profiles")
     for name in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
@@ -294,7 +311,11 @@ def main_reference(args):
     value = w.causal_flops / t_mean / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
-        "warmup": W, "ms_per_step": t_mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "warmup": W, "ms_per_step": t_mean * 1e3, "extrapolated": True,
+        "ms_per_step_note": ("extrapolated: each step times the oracle on a sample of the workload and scales "
+                             "its per-element and per-FLOP times to the full workload; the run itself takes "
+                             "about steps x the sample time"),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3 path emulated (fp32 quantiser, float64 attention)",
         "data": "synthetic (seeded Gaussian, bf16)",
         "config": {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "Dqk": w.Dqk, "Dv": w.Dv,
@@ -505,12 +526,42 @@ def main():
 
         te, _ = timed(e2e_step, max(3, min(K, 20)), 3)
         te = max_over_ranks(te, world)
+
+        # The pieces alone: inputs host -> device, output device -> host
+        # (whole tensors on one stream), next to the device step timed above.
+        def h2d_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            if ev is not None:
+                ev[1].record(stream)
+
+        def d2h_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            ho.copy_(o8, non_blocking=True)
+            if ev is not None:
+                ev[1].record(stream)
+
+        n_copy = max(3, min(K, 10))
+        t_h2d, _ = timed(h2d_step, n_copy, 2)
+        t_d2h, _ = timed(d2h_step, n_copy, 2)
+        h2d_b = sum(t.numel() * t.element_size() for t in (q, k, v))
+        d2h_b = o8.numel() * o8.element_size()
+        serial = t_h2d + t8 + t_d2h
         e2e = {"value": world * w.causal_flops / (te * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (q, k, v))),
                "d2h_bytes_per_step": int(o8.numel() * o8.element_size()), "ms_per_step": te,
                "path": "prefill_fp8_host: pinned host bf16 Q/K/V -> device, quantise + FP8 attention, "
                        "bf16 O -> pinned host, pipelined along the sequence",
-               "chunks": args.chunks}
+               "chunks": args.chunks,
+               "breakdown": {"h2d_ms": t_h2d, "h2d_GBps": h2d_b / (t_h2d * 1e-3) / 1e9,
+                             "device_ms": t8, "d2h_ms": t_d2h, "d2h_GBps": d2h_b / (t_d2h * 1e-3) / 1e9,
+                             "serial_ms": serial, "e2e_ms": te, "hidden_ms": serial - te,
+                             "note": "pieces timed alone (whole-tensor copies on one stream, the device FP8 step); "
+                                     "hidden_ms = the part of their sum the pipeline overlaps"}}
 
     paged = None
     if args.paged:
@@ -526,8 +577,24 @@ def main():
     v16 = world * w.causal_flops / (t16 * 1e-3) / 1e12
     a8 = w.causal_flops / (t8k * 1e-3) / 1e12
     a16 = w.causal_flops / (t16k * 1e-3) / 1e12
-    tr8 = traffic_from_profiles("attention.cu", f"attn_fwd_fp8:{name}")
-    tr16 = traffic_from_profiles("attention.cu", f"attn_fwd_bf16:{name}")
+    tr8 = traffic_from_profiles(ATTN_SOURCES, f"attn_fwd_fp8:{name}")
+    tr16 = traffic_from_profiles(ATTN_SOURCES, f"attn_fwd_bf16:{name}")
+    # Secondary bounds of the FP8 kernel: one exponential and one e4m3
+    # conversion per causal score, B*Hq*S^2/2 of each per launch, against the
+    # per-SM rates above at the median SM clock sampled during the timed region.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks["sm_mhz"] if clocks else peaks.get("sm_max_mhz", 2070.0)
+    n_scores = 0.5 * w.B * w.Hq * w.S * w.S
+    secondary = {
+        "scores_per_launch": n_scores, "sm_count": sms, "sm_mhz": mhz,
+        "exp2": {"achieved_per_s": n_scores / (t8k * 1e-3), "peak_per_s": EX2_PER_CLK_SM * sms * mhz * 1e6,
+                 "frac": n_scores / (t8k * 1e-3) / (EX2_PER_CLK_SM * sms * mhz * 1e6),
+                 "peak_note": f"{EX2_PER_CLK_SM:g} ex2/clk/SM (measured) x SMs x sampled clock"},
+        "e4m3_cvt": {"achieved_per_s": n_scores / (t8k * 1e-3),
+                     "peak_per_s": E4M3_CVT_PER_CLK_SM * sms * mhz * 1e6,
+                     "frac": n_scores / (t8k * 1e-3) / (E4M3_CVT_PER_CLK_SM * sms * mhz * 1e6),
+                     "peak_note": f"{E4M3_CVT_PER_CLK_SM:g} converted elements/clk/SM (measured) x SMs x sampled clock"},
+    }
 
     if rank != 0:
         return
@@ -547,9 +614,10 @@ def main():
                         "peak_source": f"{src} (fp8 = bf16 x {FP8_PER_BF16:g}, nominal ratio)"},
         "roofline": {"bound": "tensor", "achieved": a8, "peak": fp8_peak, "unit": UNIT, "frac": a8 / fp8_peak,
                      "traffic": tr8, "kernel": "attn_fwd_fp8",
-                     "peak_note": f"dense fp8 = {src} bf16 burst {peaks['bf16_tflops']:g} x {FP8_PER_BF16:g} (of {src}); "
-                                  f"sustained-peak frac {a8 / fp8_peak_sus:.3f}",
-                     "ms_per_launch": t8k},
+                     "peak_note": (f"the fp8 peak is nominal: {src} bf16 burst {peaks['bf16_tflops']:g} TFLOP/s x "
+                                   f"{FP8_PER_BF16:g}, the nominal fp8/bf16 tensor-core ratio (no fp8 figure is "
+                                   f"measured); sustained-peak frac {a8 / fp8_peak_sus:.3f}"),
+                     "ms_per_launch": t8k, "secondary": secondary},
         "bf16": {"value": v16, "unit": UNIT, "ms_per_step": t16, "dtype": "bf16", "gpu_launches": K,
                  "roofline": {"bound": "tensor", "achieved": a16, "peak": peaks["bf16_tflops"], "unit": UNIT,
                               "frac": a16 / peaks["bf16_tflops"], "traffic": tr16, "kernel": "attn_fwd_bf16",
