@@ -74,6 +74,14 @@ def lib() -> ctypes.CDLL:
     L.zyfa_quantize_fp8_rows.restype = c_int
     L.zyfa_quantize_fp8_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, c_int, c_int,
                                          c_int, c_int, c_int, c_int, c_int, vp]
+    L.zyfa_quantize_fp8_qkv.restype = c_int
+    L.zyfa_quantize_fp8_qkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp] + [c_int] * 7 + [vp]
+    L.zyfa_quantize_fp8_qkv_rows.restype = c_int
+    L.zyfa_quantize_fp8_qkv_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp] + [c_int] * 9 + [vp]
+    L.zyfa_quantize_fp8_qkv_varlen.restype = c_int
+    L.zyfa_quantize_fp8_qkv_varlen.argtypes = [vp] * 13 + [c_int] * 6 + [vp]
+    L.zyfa_quantize_fp8_qkv_varlen_dev.restype = c_int
+    L.zyfa_quantize_fp8_qkv_varlen_dev.argtypes = [vp] * 13 + [c_int] * 8 + [vp, vp]
     L.zyfa_prefill_fp8_host_workspace.restype = ctypes.c_size_t
     L.zyfa_prefill_fp8_host_workspace.argtypes = [c_int] * 6
     L.zyfa_prefill_fp8_host.restype = c_int
@@ -179,6 +187,36 @@ def quantize_fp8(x: torch.Tensor, hadamard: bool = False, out: Optional[torch.Te
     return out, scales
 
 
+def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
+                     stream: Optional[torch.cuda.Stream] = None, rows: Optional[Tuple[int, int]] = None,
+                     out=None):
+    """Q, K and V of one attention call quantised in one launch (Q and K
+    rotated when hadamard, V never): the bytes of three quantize_fp8 calls.
+    Returns ((q8, qs), (k8, ks), (v8, vs)). out: the same structure of
+    preallocated tensors to write into; rows=(begin, end) as quantize_fp8."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16)
+    B, S, Hq, Dqk = q.shape
+    Hkv, Dv = k.shape[2], v.shape[3]
+    if out is None:
+        out = tuple((torch.empty(t.shape, dtype=torch.uint8, device=t.device),
+                     torch.empty((B, t.shape[2], scale_blocks(S)), dtype=torch.float32, device=t.device))
+                    for t in (q, k, v))
+    for c, sc in out:
+        if not c.is_contiguous() or not sc.is_contiguous():
+            raise ValueError("out and scales must be contiguous")
+    (q8, qs), (k8, ks), (v8, vs) = out
+    ptrs = (q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v), q8.data_ptr(),
+            qs.data_ptr(), k8.data_ptr(), ks.data_ptr(), v8.data_ptr(), vs.data_ptr())
+    if rows is None:
+        _check(lib().zyfa_quantize_fp8_qkv(*ptrs, B, S, Hq, Hkv, Dqk, Dv, int(bool(hadamard)),
+                                           _stream_ptr(q, stream)))
+    else:
+        _check(lib().zyfa_quantize_fp8_qkv_rows(*ptrs, B, S, Hq, Hkv, Dqk, Dv, int(bool(hadamard)), int(rows[0]),
+                                                int(rows[1]), _stream_ptr(q, stream)))
+    return out
+
+
 def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: Optional[float] = None,
                   out: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None,
@@ -244,13 +282,11 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
 def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
                 softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False):
-    """The FP8 prefill path: quantise Q and K (optionally rotated) and V, then
-    FP8 attention. Returns (o, (q8, qs, k8, ks, v8, vs))."""
+    """The FP8 prefill path: quantise Q and K (optionally rotated) and V in
+    one launch, then FP8 attention. Returns (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[3])
-    q8, qs = quantize_fp8(q, hadamard, stream=stream)
-    k8, ks = quantize_fp8(k, hadamard, stream=stream)
-    v8, vs = quantize_fp8(v, False, stream=stream)
+    (q8, qs), (k8, ks), (v8, vs) = quantize_fp8_qkv(q, k, v, hadamard, stream=stream)
     o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream, lean_p=lean_p)
     return o, (q8, qs, k8, ks, v8, vs)
 
@@ -376,6 +412,36 @@ def quantize_fp8_varlen(x: torch.Tensor, cu_seqlens, hadamard: bool = False,
     return out, scales
 
 
+def quantize_fp8_qkv_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens, hadamard: bool = False,
+                            stream: Optional[torch.cuda.Stream] = None, max_seqlen: Optional[int] = None):
+    """Q, K and V of a packed variable-length batch quantised in one launch
+    (the bytes of three quantize_fp8_varlen calls). Returns ((q8, qs),
+    (k8, ks), (v8, vs)); device offsets as quantize_fp8_varlen."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require_packed(t, n, torch.bfloat16)
+    T, Hq, Dqk = q.shape
+    Hkv, Dv = k.shape[1], v.shape[2]
+    dev = _cu_device(cu_seqlens, max_seqlen, q.device)
+    if dev is not None:
+        cu_ptr, B, max_len = dev
+    else:
+        cu, B, max_len = _cu_host(cu_seqlens)
+    out = tuple((torch.empty(t.shape, dtype=torch.uint8, device=t.device),
+                 torch.zeros((B, t.shape[1], scale_blocks(max_len)), dtype=torch.float32, device=t.device))
+                for t in (q, k, v))
+    (q8, qs), (k8, ks), (v8, vs) = out
+    ptrs = (q.data_ptr(), _strides2(q), k.data_ptr(), _strides2(k), v.data_ptr(), _strides2(v), q8.data_ptr(),
+            qs.data_ptr(), k8.data_ptr(), ks.data_ptr(), v8.data_ptr(), vs.data_ptr())
+    if dev is not None:
+        ws = _varlen_workspace(q.device, stream)
+        _check(lib().zyfa_quantize_fp8_qkv_varlen_dev(*ptrs, cu_ptr, B, T, max_len, Hq, Hkv, Dqk, Dv,
+                                                      int(bool(hadamard)), ws.data_ptr(), _stream_ptr(q, stream)))
+    else:
+        _check(lib().zyfa_quantize_fp8_qkv_varlen(*ptrs, cu, B, Hq, Hkv, Dqk, Dv, int(bool(hadamard)),
+                                                  _stream_ptr(q, stream)))
+    return out
+
+
 def attn_fwd_bf16_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens,
                          softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                          stream: Optional[torch.cuda.Stream] = None,
@@ -494,9 +560,8 @@ def prefill_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seq
     (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[2])
-    q8, qs = quantize_fp8_varlen(q, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
-    k8, ks = quantize_fp8_varlen(k, cu_seqlens, hadamard, stream=stream, max_seqlen=max_seqlen)
-    v8, vs = quantize_fp8_varlen(v, cu_seqlens, False, stream=stream, max_seqlen=max_seqlen)
+    (q8, qs), (k8, ks), (v8, vs) = quantize_fp8_qkv_varlen(q, k, v, cu_seqlens, hadamard, stream=stream,
+                                                           max_seqlen=max_seqlen)
     o = attn_fwd_fp8_varlen(q8, qs, k8, ks, v8, vs, cu_seqlens, softmax_scale, stream=stream, max_seqlen=max_seqlen,
                             lean_p=lean_p)
     return o, (q8, qs, k8, ks, v8, vs)

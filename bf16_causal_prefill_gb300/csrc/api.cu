@@ -207,66 +207,132 @@ int zyfa_set_debug(int stall_loader, double timeout_seconds) {
   return ZYFA_OK;
 }
 
-static int quant_common(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
-                        float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
-                        void* stream) {
-  if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
-  if (B < 1 || S < 1 || H < 1) return fail(ZYFA_ERR_INVALID_ARG, "B, S, H must be >= 1");
+// One tensor of a quantiser call.
+struct QuantIn {
+  const void* x;            // bf16
+  int64_t sb, ss, sh;       // element strides of x (packed: sb unused)
+  void* out;                // e4m3 codes, dense
+  float* scales;
+  int H, D, hadamard;
+  const char* name;
+};
+
+static int check_quant_in(const QuantIn& t) {
+  if (!t.x || !t.out || !t.scales) return fail(ZYFA_ERR_INVALID_ARG, "%s: null pointer", t.name);
+  if (t.H < 1 || t.H > 65535) return fail(ZYFA_ERR_INVALID_ARG, "%s: H must be in 1..65535", t.name);
+  if (t.D != 128 && t.D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "%s: head dim %d unsupported (128 or 192)", t.name, t.D);
+  if (t.hadamard && t.D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "%s: Hadamard rotation needs head dim 128", t.name);
+  if (!aligned(t.x, 4) || !aligned(t.out, 2) || !aligned(t.scales, 4))
+    return fail(ZYFA_ERR_INVALID_ARG, "%s: misaligned pointer", t.name);
+  if (t.sb <= 0 || t.ss <= 0 || t.sh <= 0 || (t.sb | t.ss | t.sh) & 1)
+    return fail(ZYFA_ERR_INVALID_ARG, "%s: strides must be positive and even", t.name);
+  return ZYFA_OK;
+}
+
+// Inputs whose base and strides allow 16-byte tiled copies go to the
+// streaming kernel; other views to the register kernel (same bytes).
+static bool quant_tileable(const QuantIn& t) {
+  const int64_t lim = int64_t(1) << 38;
+  return aligned(t.x, 16) && aligned(t.out, 16) && t.sb % 8 == 0 && t.ss % 8 == 0 && t.sh % 8 == 0 && t.sb < lim &&
+         t.ss < lim && t.sh < lim;
+}
+
+static int quant_stream_tensor(const QuantIn& t, int B, int S, zyfa::QuantMaps* m, zyfa::QuantStreamArgs* a, int i) {
+  const int64_t xs[3] = {t.sb, t.ss, t.sh};
+  const int64_t os[3] = {static_cast<int64_t>(S) * t.H * t.D, static_cast<int64_t>(t.H) * t.D, t.D};
+  int r = make_map(&m->in[i], t.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.D, t.H, S, B, xs, t.name);
+  if (!r) r = make_map(&m->out[i], t.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, t.D, t.H, S, B, os, t.name);
+  if (r) return r;
+  a->t[i].out = static_cast<uint8_t*>(t.out);
+  a->t[i].scales = t.scales;
+  a->t[i].H = t.H;
+  a->t[i].D = t.D;
+  a->t[i].hadamard = t.hadamard;
+  return ZYFA_OK;
+}
+
+// Equal-length tensors [B,S,H_t,D_t], 128-token blocks covering rows
+// [row_begin, row_end): one streaming launch for all of them when every
+// tensor can be tiled, else one launch per tensor.
+static int quant_dense(const QuantIn* in, int n, int B, int S, int row_begin, int row_end, void* stream) {
+  if (B < 1 || S < 1) return fail(ZYFA_ERR_INVALID_ARG, "B, S, H must be >= 1");
   if (row_begin < 0 || row_end > S || row_begin >= row_end || row_begin % 128 != 0 ||
       (row_end != S && row_end % 128 != 0))
     return fail(ZYFA_ERR_INVALID_ARG, "row range [%d, %d) must be non-empty, inside [0, %d), on 128-token blocks",
                 row_begin, row_end, S);
-  if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
-  if (hadamard && D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
-  if (!aligned(x, 4) || !aligned(out, 2) || !aligned(scales, 4))
-    return fail(ZYFA_ERR_INVALID_ARG, "misaligned pointer");
-  if (stride_b <= 0 || stride_s <= 0 || stride_h <= 0 || (stride_b | stride_s | stride_h) & 1)
-    return fail(ZYFA_ERR_INVALID_ARG, "strides must be positive and even");
-  if ((static_cast<long long>(S) + 127) / 128 > 65535 * 1024LL || H > 65535 || B > 65535)
+  if ((static_cast<long long>(S) + 127) / 128 > 65535 * 1024LL || B > 65535)
     return fail(ZYFA_ERR_INVALID_ARG, "grid too large");
+  bool all_tile = true;
+  for (int t = 0; t < n; ++t) {
+    if (int r = check_quant_in(in[t])) return r;
+    all_tile = all_tile && quant_tileable(in[t]);
+  }
   DeviceInfo* d;
   if (int r = device_info(&d)) return r;
-  zyfa::QuantArgs a{};
-  a.x = x;
-  a.sb = stride_b;
-  a.ss = stride_s;
-  a.sh = stride_h;
-  a.out = static_cast<uint8_t*>(out);
-  a.scales = scales;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  zyfa::QuantStreamArgs a{};
   a.B = B;
   a.S = S;
-  a.H = H;
-  a.D = D;
   a.blk_lo = row_begin / 128;
   a.blk_hi = (row_end + 127) / 128;
-  a.hadamard = hadamard;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns;
-  a.num_sms = d->sm_count;
-  cudaError_t e;
-  // TMA streaming kernel when the input allows 16-byte tiled copies; the
-  // register kernel otherwise. Both produce the same bytes.
-  const bool tma_ok = aligned(x, 16) && aligned(out, 16) && stride_b % 8 == 0 && stride_s % 8 == 0 &&
-                      stride_h % 8 == 0 && stride_b < (int64_t(1) << 38) && stride_s < (int64_t(1) << 38) &&
-                      stride_h < (int64_t(1) << 38);
-  if (tma_ok) {
-    CUtensorMap tm;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
-                                static_cast<cuuint64_t>(B)};
-    const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(stride_h) * 2, static_cast<cuuint64_t>(stride_s) * 2,
-                                    static_cast<cuuint64_t>(stride_b) * 2};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1u, 128u, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    CUresult cr = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, gstrides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(x) failed: %d", (int)cr);
-    e = zyfa::launch_quantize_fp8_stream(tm, a, static_cast<cudaStream_t>(stream));
-  } else {
-    e = zyfa::launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+  for (int t0 = 0; t0 < n; t0 = all_tile ? n : t0 + 1) {
+    const int t1 = all_tile ? n : t0 + 1;
+    cudaError_t e;
+    if (quant_tileable(in[t0])) {
+      zyfa::QuantMaps m{};
+      int dmax = 128;
+      for (int t = t0; t < t1; ++t) {
+        if (int r = quant_stream_tensor(in[t], B, S, &m, &a, t - t0)) return r;
+        dmax = std::max(dmax, in[t].D);
+      }
+      a.n = t1 - t0;
+      e = zyfa::launch_quantize_fp8_stream(m, a, dmax, d->sm_count, st);
+    } else {
+      const QuantIn& t = in[t0];
+      zyfa::QuantArgs r{};
+      r.x = t.x;
+      r.sb = t.sb;
+      r.ss = t.ss;
+      r.sh = t.sh;
+      r.out = static_cast<uint8_t*>(t.out);
+      r.scales = t.scales;
+      r.B = B;
+      r.S = S;
+      r.H = t.H;
+      r.D = t.D;
+      r.blk_lo = a.blk_lo;
+      r.blk_hi = a.blk_hi;
+      r.hadamard = t.hadamard;
+      r.status = d->status;
+      r.timeout_ns = g_timeout_ns;
+      r.num_sms = d->sm_count;
+      e = zyfa::launch_quantize_fp8(r, st);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8 launch");
   }
-  if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8 launch");
   return ZYFA_OK;
+}
+
+static int quant_common(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
+                        float* scales, int B, int S, int H, int D, int hadamard, int row_begin, int row_end,
+                        void* stream) {
+  const QuantIn t{x, stride_b, stride_s, stride_h, out, scales, H, D, hadamard, "x"};
+  return quant_dense(&t, 1, B, S, row_begin, row_end, stream);
+}
+
+static int quant_qkv(const void* q, const int64_t qs[3], const void* k, const int64_t ks[3], const void* v,
+                     const int64_t vs[3], void* q8, float* q_scale, void* k8, float* k_scale, void* v8,
+                     float* v_scale, int B, int S, int Hq, int Hkv, int Dqk, int Dv, int hadamard, int row_begin,
+                     int row_end, void* stream) {
+  if (!qs || !ks || !vs) return fail(ZYFA_ERR_INVALID_ARG, "null strides pointer");
+  if (!((Dqk == 128 || Dqk == 192) && Dv == 128))
+    return fail(ZYFA_ERR_UNSUPPORTED, "head dims (%d, %d) unsupported; use (128, 128) or (192, 128)", Dqk, Dv);
+  const QuantIn in[3] = {{q, qs[0], qs[1], qs[2], q8, q_scale, Hq, Dqk, hadamard, "q"},
+                         {k, ks[0], ks[1], ks[2], k8, k_scale, Hkv, Dqk, hadamard, "k"},
+                         {v, vs[0], vs[1], vs[2], v8, v_scale, Hkv, Dv, 0, "v"}};
+  return quant_dense(in, 3, B, S, row_begin, row_end, stream);
 }
 
 int zyfa_quantize_fp8(const void* x, int64_t stride_b, int64_t stride_s, int64_t stride_h, void* out,
@@ -279,6 +345,22 @@ int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, in
                            void* stream) {
   return quant_common(x, stride_b, stride_s, stride_h, out, scales, B, S, H, D, hadamard, row_begin, row_end,
                       stream);
+}
+
+int zyfa_quantize_fp8_qkv(const void* q, const int64_t q_strides[3], const void* k, const int64_t k_strides[3],
+                          const void* v, const int64_t v_strides[3], void* q8, float* q_scale, void* k8,
+                          float* k_scale, void* v8, float* v_scale, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
+                          int hadamard, void* stream) {
+  return quant_qkv(q, q_strides, k, k_strides, v, v_strides, q8, q_scale, k8, k_scale, v8, v_scale, B, S, Hq, Hkv,
+                   Dqk, Dv, hadamard, 0, S, stream);
+}
+
+int zyfa_quantize_fp8_qkv_rows(const void* q, const int64_t q_strides[3], const void* k, const int64_t k_strides[3],
+                               const void* v, const int64_t v_strides[3], void* q8, float* q_scale, void* k8,
+                               float* k_scale, void* v8, float* v_scale, int B, int S, int Hq, int Hkv, int Dqk,
+                               int Dv, int hadamard, int row_begin, int row_end, void* stream) {
+  return quant_qkv(q, q_strides, k, k_strides, v, v_strides, q8, q_scale, k8, k_scale, v8, v_scale, B, S, Hq, Hkv,
+                   Dqk, Dv, hadamard, row_begin, row_end, stream);
 }
 
 // Work order of the equal-length kernels: how many (batch, KV head) groups
@@ -819,8 +901,11 @@ int zyfa_attn_decode_fp8_paged(const void* q8, const float* q_scale, const void*
                      v_cache_strides, o_strides, workspace, workspace_bytes, stream);
 }
 
-static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
-                        const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream,
+// Packed variable-length tensors [T,H_t,D_t] (token strides in in[t].ss,
+// head strides in in[t].sh): one streaming launch for all of them. Offsets
+// on the host (cu_seqlens) or on the device (cu_dev, with the packed token
+// count, a bound on the sequence length and the workspace for the table).
+static int quant_packed(const QuantIn* in_, int n, const int32_t* cu_seqlens, int B, void* stream,
                         const int32_t* cu_dev = nullptr, int total_dev = 0, int max_len_dev = 0,
                         void* workspace = nullptr) {
   int T = 0, max_len = 0;
@@ -831,50 +916,38 @@ static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void*
   } else if (int r = read_seqlens(cu_seqlens, B, &T, &max_len)) {
     return r;
   }
-  if (!x || !out || !scales) return fail(ZYFA_ERR_INVALID_ARG, "null pointer");
-  if (H < 1 || H > 65535) return fail(ZYFA_ERR_INVALID_ARG, "H must be in 1..65535");
-  if (D != 128 && D != 192) return fail(ZYFA_ERR_UNSUPPORTED, "head dim %d unsupported (128 or 192)", D);
-  if (hadamard && D != 128) return fail(ZYFA_ERR_UNSUPPORTED, "Hadamard rotation needs head dim 128");
-  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(scales, 4) || stride_t <= 0 || stride_h <= 0 ||
-      stride_t % 8 != 0 || stride_h % 8 != 0 || stride_t >= (int64_t(1) << 38) || stride_h >= (int64_t(1) << 38))
-    return fail(ZYFA_ERR_UNSUPPORTED,
-                "packed input needs 16-byte aligned x/out and token/head strides that are multiples of 8 elements");
+  QuantIn in[3];
+  int dmax = 128;
+  for (int t = 0; t < n; ++t) {
+    in[t] = in_[t];
+    in[t].sb = in[t].ss * std::max(T, 1);
+    if (int r = check_quant_in(in[t])) return r;
+    if (!quant_tileable(in[t]))
+      return fail(ZYFA_ERR_UNSUPPORTED,
+                  "%s: packed input needs 16-byte aligned x/out and token/head strides that are multiples of 8 "
+                  "elements", in[t].name);
+    dmax = std::max(dmax, in[t].D);
+  }
   if (T == 0) return ZYFA_OK;
   DeviceInfo* d;
   if (int r = device_info(&d)) return r;
-  zyfa::QuantArgs a{};
-  a.x = x;
-  a.sb = stride_t * T;
-  a.ss = stride_t;
-  a.sh = stride_h;
-  a.out = static_cast<uint8_t*>(out);
-  a.scales = scales;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  zyfa::QuantMaps m{};
+  zyfa::QuantStreamArgs a{};
+  for (int t = 0; t < n; ++t)
+    if (int r = quant_stream_tensor(in[t], 1, T, &m, &a, t)) return r;
+  a.n = n;
   a.B = 1;
   a.S = T;
-  a.H = H;
-  a.D = D;
   a.blk_lo = 0;
   a.blk_hi = (T + 127) / 128;
-  a.hadamard = hadamard;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns;
-  a.num_sms = d->sm_count;
-  CUtensorMap tm;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 1};
-  const cuuint64_t gstrides[3] = {static_cast<cuuint64_t>(stride_h) * 2, static_cast<cuuint64_t>(stride_t) * 2,
-                                  static_cast<cuuint64_t>(stride_t) * 2 * static_cast<cuuint64_t>(T)};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1u, 128u, 1u};
-  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult cr = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, gstrides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return fail(ZYFA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled(x) failed: %d", (int)cr);
   if (cu_dev) {
     auto* dtab = reinterpret_cast<zyfa::QuantSeqTable*>(static_cast<char*>(workspace) + varlen_ws_quant_offset());
-    cudaError_t e = zyfa::launch_build_seq_tables(cu_dev, B, T, max_len, H, nullptr, dtab, d->status,
-                                                  static_cast<cudaStream_t>(stream));
+    cudaError_t e = zyfa::launch_build_seq_tables(cu_dev, B, T, max_len, in[0].H, nullptr, dtab, d->status, st);
     if (e != cudaSuccess) return fail_cuda(e, "build_seq_tables launch");
-    e = zyfa::launch_quantize_fp8_stream_varlen_dev(tm, a, dtab, static_cast<cudaStream_t>(stream));
+    e = zyfa::launch_quantize_fp8_stream_varlen_dev(m, a, dmax, dtab, d->sm_count, st);
     if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
     return ZYFA_OK;
   }
@@ -887,9 +960,31 @@ static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void*
     tab.len[i] = cu_seqlens[i + 1] - cu_seqlens[i];
     tab.cum_blocks[i + 1] = tab.cum_blocks[i] + (tab.len[i] + 127) / 128;
   }
-  cudaError_t e = zyfa::launch_quantize_fp8_stream_varlen(tm, a, tab, static_cast<cudaStream_t>(stream));
+  cudaError_t e = zyfa::launch_quantize_fp8_stream_varlen(m, a, dmax, tab, d->sm_count, st);
   if (e != cudaSuccess) return fail_cuda(e, "quantize_fp8_varlen launch");
   return ZYFA_OK;
+}
+
+static int quant_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
+                        const int32_t* cu_seqlens, int B, int H, int D, int hadamard, void* stream,
+                        const int32_t* cu_dev = nullptr, int total_dev = 0, int max_len_dev = 0,
+                        void* workspace = nullptr) {
+  const QuantIn t{x, 0, stride_t, stride_h, out, scales, H, D, hadamard, "x"};
+  return quant_packed(&t, 1, cu_seqlens, B, stream, cu_dev, total_dev, max_len_dev, workspace);
+}
+
+static int quant_qkv_packed(const void* q, const int64_t qs[2], const void* k, const int64_t ks[2], const void* v,
+                            const int64_t vs[2], void* q8, float* q_scale, void* k8, float* k_scale, void* v8,
+                            float* v_scale, const int32_t* cu_seqlens, int B, int Hq, int Hkv, int Dqk, int Dv,
+                            int hadamard, void* stream, const int32_t* cu_dev = nullptr, int total_dev = 0,
+                            int max_len_dev = 0, void* workspace = nullptr) {
+  if (!qs || !ks || !vs) return fail(ZYFA_ERR_INVALID_ARG, "null strides pointer");
+  if (!((Dqk == 128 || Dqk == 192) && Dv == 128))
+    return fail(ZYFA_ERR_UNSUPPORTED, "head dims (%d, %d) unsupported; use (128, 128) or (192, 128)", Dqk, Dv);
+  const QuantIn in[3] = {{q, 0, qs[0], qs[1], q8, q_scale, Hq, Dqk, hadamard, "q"},
+                         {k, 0, ks[0], ks[1], k8, k_scale, Hkv, Dqk, hadamard, "k"},
+                         {v, 0, vs[0], vs[1], v8, v_scale, Hkv, Dv, 0, "v"}};
+  return quant_packed(in, 3, cu_seqlens, B, stream, cu_dev, total_dev, max_len_dev, workspace);
 }
 
 int zyfa_quantize_fp8_varlen(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
@@ -904,6 +999,25 @@ int zyfa_quantize_fp8_varlen_dev(const void* x, int64_t stride_t, int64_t stride
                                  int hadamard, void* workspace, void* stream) {
   return quant_varlen(x, stride_t, stride_h, out, scales, nullptr, B, H, D, hadamard, stream, cu_seqlens_dev,
                       total_tokens, max_seqlen, workspace);
+}
+
+int zyfa_quantize_fp8_qkv_varlen(const void* q, const int64_t q_strides[2], const void* k,
+                                 const int64_t k_strides[2], const void* v, const int64_t v_strides[2], void* q8,
+                                 float* q_scale, void* k8, float* k_scale, void* v8, float* v_scale,
+                                 const int32_t* cu_seqlens, int B, int Hq, int Hkv, int Dqk, int Dv, int hadamard,
+                                 void* stream) {
+  return quant_qkv_packed(q, q_strides, k, k_strides, v, v_strides, q8, q_scale, k8, k_scale, v8, v_scale,
+                          cu_seqlens, B, Hq, Hkv, Dqk, Dv, hadamard, stream);
+}
+
+int zyfa_quantize_fp8_qkv_varlen_dev(const void* q, const int64_t q_strides[2], const void* k,
+                                     const int64_t k_strides[2], const void* v, const int64_t v_strides[2], void* q8,
+                                     float* q_scale, void* k8, float* k_scale, void* v8, float* v_scale,
+                                     const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen, int Hq,
+                                     int Hkv, int Dqk, int Dv, int hadamard, void* workspace, void* stream) {
+  return quant_qkv_packed(q, q_strides, k, k_strides, v, v_strides, q8, q_scale, k8, k_scale, v8, v_scale, nullptr,
+                          B, Hq, Hkv, Dqk, Dv, hadamard, stream, cu_seqlens_dev, total_tokens, max_seqlen,
+                          workspace);
 }
 
 int zyfa_attn_fwd_bf16_varlen_dev(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens_dev,
@@ -1150,9 +1264,8 @@ int zyfa_prefill_fp8_host(const void* q, const void* k, const void* v, void* o, 
     // SMs that the tail of this one leaves idle (pieces depend only on the
     // quantised inputs, never on each other's outputs).
     cudaStream_t sa = p->att[c % kAttnStreams];
-    if ((rc = quant_common(qd, sq[0], sq[1], sq[2], q8, qs, B, S, Hq, Dqk, hadamard, r0, r1, stream)) ||
-        (rc = quant_common(kd, sk[0], sk[1], sk[2], k8, ks, B, S, Hkv, Dqk, hadamard, r0, r1, stream)) ||
-        (rc = quant_common(vd, sv[0], sv[1], sv[2], v8, vs, B, S, Hkv, Dv, 0, r0, r1, stream)))
+    if ((rc = quant_qkv(qd, sq, kd, sk, vd, sv, q8, qs, k8, ks, v8, vs, B, S, Hq, Hkv, Dqk, Dv, hadamard, r0, r1,
+                        stream)))
       break;
     if ((e = cudaEventRecord(p->quant[c], st)) != cudaSuccess || (e = cudaStreamWaitEvent(sa, p->quant[c], 0)) != cudaSuccess) {
       rc = fail_cuda(e, "host pipeline: order attention");

@@ -39,14 +39,37 @@ struct QuantSeqTable {
 
 // Register kernel: any 4-byte aligned input with even strides.
 cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
-// Streaming kernel: persistent CTAs, TMA ring of input blocks. tm_x is a 4-D
-// map (D, H, S, B) over x, no swizzle, box D x 1 x 128 x 1 (needs a 16-byte
-// aligned base and strides that are multiples of 8 elements).
-cudaError_t launch_quantize_fp8_stream(const CUtensorMap& tm_x, const QuantArgs& a, cudaStream_t stream);
-// Streaming kernel over a packed variable-length tensor (B = 1, S = total
-// tokens in `a`; tm_x over (D, H, T, 1)).
-cudaError_t launch_quantize_fp8_stream_varlen(const CUtensorMap& tm_x, const QuantArgs& a, const QuantSeqTable& tab,
-                                              cudaStream_t stream);
+
+// Streaming kernel: up to three tensors of one call (Q, K, V) in one launch.
+struct QuantTensor {
+  uint8_t* out;           // e4m3 [B,S,H,D] dense (packed: [T,H,D])
+  float* scales;          // [B,H,ceil(S/128)] (packed: [n_seqs,H,max_blocks])
+  int H, D;               // heads; head dim 128 or 192
+  int hadamard;           // rotate rows before quantising (D = 128 only)
+};
+struct QuantStreamArgs {
+  QuantTensor t[3];
+  int n;                  // tensors of the call, 1 to 3
+  int B, S;               // packed: B = 1, S = total tokens
+  int blk_lo, blk_hi;     // equal lengths: 128-token blocks [blk_lo, blk_hi) of every tensor
+  unsigned int* status;   // device status word (bounded waits)
+  uint64_t timeout_ns;
+};
+// in[t]: bf16 5-D map (64, S, D/64, H, B) over tensor t, box 64 x 128 x D/64
+// x 1 x 1, 128-byte swizzle (16-byte aligned base, strides multiples of 8
+// elements). out[t]: the e4m3 output, D = 128: 5-D map (128, S, 1, H, B),
+// box 128 x 128 x 1 x 1 x 1; D = 192: 4-D map (D, H, S, B), box 128 x 1 x
+// 128 x 1; both 128-byte swizzle.
+struct QuantMaps {
+  CUtensorMap in[3];
+  CUtensorMap out[3];
+};
+// dmax: the largest head dim of the call's tensors.
+cudaError_t launch_quantize_fp8_stream(const QuantMaps& m, const QuantStreamArgs& a, int dmax, int num_sms,
+                                       cudaStream_t stream);
+// Packed variable-length tensors (B = 1, S = total tokens; maps over T).
+cudaError_t launch_quantize_fp8_stream_varlen(const QuantMaps& m, const QuantStreamArgs& a, int dmax,
+                                              const QuantSeqTable& tab, int num_sms, cudaStream_t stream);
 
 // Variable-length batches: sequences packed along the token dimension. The
 // host sorts the sequences by length (longest first) and lays out the unit
@@ -143,7 +166,7 @@ cudaError_t launch_attn_bf16_varlen_dev(const CUtensorMap& tm_q, const CUtensorM
                                         const AttnArgs& a, const SeqTable* tab, cudaStream_t stream);
 cudaError_t launch_attn_fp8_varlen_dev(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                        const AttnArgs& a, const SeqTable* tab, cudaStream_t stream);
-cudaError_t launch_quantize_fp8_stream_varlen_dev(const CUtensorMap& tm_x, const QuantArgs& a,
-                                                  const QuantSeqTable* tab, cudaStream_t stream);
+cudaError_t launch_quantize_fp8_stream_varlen_dev(const QuantMaps& m, const QuantStreamArgs& a, int dmax,
+                                                  const QuantSeqTable* tab, int num_sms, cudaStream_t stream);
 
 }  // namespace zyfa

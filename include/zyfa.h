@@ -109,6 +109,32 @@ int zyfa_quantize_fp8_rows(const void* x, int64_t stride_b, int64_t stride_s, in
                            void* stream);
 
 /*
+ * Q, K and V of one attention call quantised in one launch: the same bytes
+ * as three zyfa_quantize_fp8 calls, Q and K with the rotation when
+ * hadamard != 0, V never rotated ("ZYFA ...", "FP8 Error in Full-Model
+ * Inference": the rotation cancels in Q K^T, so only Q and K take it).
+ *
+ * q, k, v     : bf16 [B,S,Hq,Dqk], [B,S,Hkv,Dqk], [B,S,Hkv,Dv]; strides
+ *               (batch, token, head) in elements.
+ * q8, k8, v8  : uint8 e4m3 codes, dense, same shapes, caller-allocated.
+ * *_scale     : float [B,H,ceil(S/128)] for each, caller-allocated.
+ * (Dqk, Dv)   : (128, 128) or (192, 128); hadamard requires Dqk == 128.
+ * When all three inputs allow 16-byte tiled copies (16-byte aligned bases,
+ * strides multiples of 8 elements) this is one launch; otherwise each
+ * tensor is quantised by its own launch (same bytes). Errors as
+ * zyfa_quantize_fp8.
+ */
+int zyfa_quantize_fp8_qkv(const void* q, const int64_t q_strides[3], const void* k, const int64_t k_strides[3],
+                          const void* v, const int64_t v_strides[3], void* q8, float* q_scale, void* k8,
+                          float* k_scale, void* v8, float* v_scale, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
+                          int hadamard, void* stream);
+/* Row-range form (rows [row_begin, row_end) as zyfa_quantize_fp8_rows). */
+int zyfa_quantize_fp8_qkv_rows(const void* q, const int64_t q_strides[3], const void* k, const int64_t k_strides[3],
+                               const void* v, const int64_t v_strides[3], void* q8, float* q_scale, void* k8,
+                               float* k_scale, void* v8, float* v_scale, int B, int S, int Hq, int Hkv, int Dqk,
+                               int Dv, int hadamard, int row_begin, int row_end, void* stream);
+
+/*
  * Causal attention, BF16 in and out ("ZYFA ..." Introduction; grouped-query
  * heads: query head h reads KV head h / (Hq / Hkv)):
  *   O[b,i,h,:] = sum_{j<=i} softmax_j(softmax_scale * Q[b,i,h].K[b,j,g]) V[b,j,g]
@@ -278,6 +304,24 @@ size_t zyfa_varlen_workspace_bytes(void);
 int zyfa_quantize_fp8_varlen_dev(const void* x, int64_t stride_t, int64_t stride_h, void* out, float* scales,
                                  const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen, int H, int D,
                                  int hadamard, void* workspace, void* stream);
+/*
+ * Q, K and V of a packed variable-length batch quantised in one launch
+ * (the bytes of three zyfa_quantize_fp8_varlen / _varlen_dev calls; Q and K
+ * rotated when hadamard != 0, V never). Strides (token, head) in elements;
+ * scales [B, H, ceil(max_len/128)]; inputs must allow 16-byte tiled copies
+ * (ZYFA_ERR_UNSUPPORTED otherwise). The _dev form takes device offsets as
+ * zyfa_quantize_fp8_varlen_dev.
+ */
+int zyfa_quantize_fp8_qkv_varlen(const void* q, const int64_t q_strides[2], const void* k,
+                                 const int64_t k_strides[2], const void* v, const int64_t v_strides[2], void* q8,
+                                 float* q_scale, void* k8, float* k_scale, void* v8, float* v_scale,
+                                 const int32_t* cu_seqlens, int B, int Hq, int Hkv, int Dqk, int Dv, int hadamard,
+                                 void* stream);
+int zyfa_quantize_fp8_qkv_varlen_dev(const void* q, const int64_t q_strides[2], const void* k,
+                                     const int64_t k_strides[2], const void* v, const int64_t v_strides[2], void* q8,
+                                     float* q_scale, void* k8, float* k_scale, void* v8, float* v_scale,
+                                     const int32_t* cu_seqlens_dev, int B, int total_tokens, int max_seqlen, int Hq,
+                                     int Hkv, int Dqk, int Dv, int hadamard, void* workspace, void* stream);
 int zyfa_attn_fwd_bf16_varlen_dev(const void* q, const void* k, const void* v, void* o, const int32_t* cu_seqlens_dev,
                                   int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int Dqk, int Dv,
                                   float softmax_scale, const int64_t q_strides[2], const int64_t k_strides[2],
