@@ -61,6 +61,9 @@ def parse_args():
     p.add_argument("--hadamard", action="store_true", help="rotate Q and K before quantisation")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--graph", action="store_true",
+                   help="also time the FP8 step and the BF16 call replayed from CUDA graphs (no host work "
+                        "between launches: the device time of small workloads)")
     p.add_argument("--chunks", type=int, default=0,
                    help="pieces of the host pipeline along the sequence (0: the library's default)")
     p.add_argument("--paged", action="store_true",
@@ -424,6 +427,42 @@ def run_decode(args, w, timed, dev):
             "path": "decode calls: one unit per (sequence, KV head), the group's query heads as tile rows"}
 
 
+def run_graph(fp8_step, bf16_step, flush, K, w, world):
+    """The FP8 step and the BF16 call captured once into CUDA graphs and
+    replayed K times each (L2 flushed between replays, CUDA events around
+    each replay): the device time without the host's per-call work."""
+    import torch
+    import bf16_causal_prefill_gb300 as zyfa
+    res = {}
+    for name, step in (("fp8_step", fp8_step), ("bf16", bf16_step)):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(K):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = max_over_ranks(sum(ts) / len(ts), world)
+        res[name] = {"ms": ms, "value": world * w.causal_flops / (ms * 1e-3) / 1e12, "unit": UNIT}
+        zyfa.device_status()
+    res["note"] = "one graph per path, replayed; the gap to the eager timing is host work per call"
+    return res
+
+
 def main():
     args = parse_args()
     if args.cpu_worker:
@@ -562,6 +601,10 @@ def main():
                              "note": "pieces timed alone (whole-tensor copies on one stream, the device FP8 step); "
                                      "hidden_ms = the part of their sum the pipeline overlaps"}}
 
+    graph = None
+    if args.graph:
+        graph = run_graph(fp8_step, bf16_step, flush, K, w, world)
+
     paged = None
     if args.paged:
         paged = run_paged(args, w, qd, kd, vd, timed, dev)
@@ -624,6 +667,7 @@ def main():
                                            f"{a16 / peaks['bf16_tflops_sustained']:.3f}"}},
         "gpu_launches": 2 * K,
         **({"paged": paged} if paged is not None else {}),
+        **({"graph": graph} if graph is not None else {}),
         **({"decode": decode} if decode is not None else {}),
         "clocks": clocks,
         "e2e": e2e,
