@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--hadamard", action="store_true", help="rotate Q and K before quantisation")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-split", action="store_true",
+                   help="small problems: keep one CTA per query-tile pair (no split key ranges)")
     p.add_argument("--graph", action="store_true",
                    help="also time the FP8 step and the BF16 call replayed from CUDA graphs (no host work "
                         "between launches: the device time of small workloads)")
@@ -502,19 +504,24 @@ def main():
     o16 = torch.empty_like(o8)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # Small problems split each query-tile pair's keys across CTAs (the
+    # library decides; this workspace lets it): allocated once, outside the
+    # timed steps. Large problems need none and run the unsplit kernels.
+    ws_bytes = 0 if args.no_split else zyfa.lib().zyfa_attn_workspace_bytes(w.B, w.S, w.Hq)
+    split_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else False
 
     def fp8_step(ev_attn=None):
         zyfa.quantize_fp8_qkv(qd, kd, vd, had, out=((q8, qs), (k8, ks), (v8, vs)))
         if ev_attn is not None:
             ev_attn[0].record(stream)
-        zyfa.attn_fwd_fp8(q8, qs, k8, ks, v8, vs, w.softmax_scale, out=o8)
+        zyfa.attn_fwd_fp8(q8, qs, k8, ks, v8, vs, w.softmax_scale, out=o8, split=split_ws)
         if ev_attn is not None:
             ev_attn[1].record(stream)
 
     def bf16_step(ev_attn=None):
         if ev_attn is not None:
             ev_attn[0].record(stream)
-        zyfa.attn_fwd_bf16(qd, kd, vd, w.softmax_scale, out=o16)
+        zyfa.attn_fwd_bf16(qd, kd, vd, w.softmax_scale, out=o16, split=split_ws)
         if ev_attn is not None:
             ev_attn[1].record(stream)
 
@@ -648,7 +655,10 @@ def main():
         "ms_per_step": t8, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3", "data": "synthetic (seeded Gaussian N(0,1), drawn in bf16, quantised per 128-token block)",
         "config": {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "Dqk": w.Dqk, "Dv": w.Dv,
-                   "path": "fp8: quantise Q,K,V (1 launch) + fp8 causal attention (1 launch)",
+                   "path": ("fp8: quantise Q,K,V (1 launch) + fp8 causal attention with key ranges split "
+                            "across CTAs (2 launches: chunks, combine)" if ws_bytes else
+                            "fp8: quantise Q,K,V (1 launch) + fp8 causal attention (1 launch)"),
+                   "split_key_ranges": bool(ws_bytes),
                    "hadamard": had, "parallelism": f"replicas x{world}",
                    "l2": "256 MiB flush between timed steps; inputs larger than L2"},
         "pct_of_peak": {"fp8_attention_kernel": a8 / fp8_peak, "fp8_step": v8 / world / fp8_peak,
@@ -660,12 +670,12 @@ def main():
                                    f"{FP8_PER_BF16:g}, the nominal fp8/bf16 tensor-core ratio (no fp8 figure is "
                                    f"measured); sustained-peak frac {a8 / fp8_peak_sus:.3f}"),
                      "ms_per_launch": t8k, "secondary": secondary},
-        "bf16": {"value": v16, "unit": UNIT, "ms_per_step": t16, "dtype": "bf16", "gpu_launches": K,
+        "bf16": {"value": v16, "unit": UNIT, "ms_per_step": t16, "dtype": "bf16", "gpu_launches": (2 if ws_bytes else 1) * K,
                  "roofline": {"bound": "tensor", "achieved": a16, "peak": peaks["bf16_tflops"], "unit": UNIT,
                               "frac": a16 / peaks["bf16_tflops"], "traffic": tr16, "kernel": "attn_fwd_bf16",
                               "peak_note": f"bf16 burst (of {src}); sustained-peak frac "
                                            f"{a16 / peaks['bf16_tflops_sustained']:.3f}"}},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (3 if ws_bytes else 2) * K,
         **({"paged": paged} if paged is not None else {}),
         **({"graph": graph} if graph is not None else {}),
         **({"decode": decode} if decode is not None else {}),

@@ -71,6 +71,14 @@ def lib() -> ctypes.CDLL:
     L.zyfa_attn_fwd_fp8_rows.restype = c_int
     L.zyfa_attn_fwd_fp8_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
                                          c_float, vp, vp, vp, vp, c_int, c_int, c_int, vp]
+    L.zyfa_attn_workspace_bytes.restype = ctypes.c_size_t
+    L.zyfa_attn_workspace_bytes.argtypes = [c_int, c_int, c_int]
+    L.zyfa_attn_fwd_bf16_ws.restype = c_int
+    L.zyfa_attn_fwd_bf16_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                        vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.zyfa_attn_fwd_fp8_ws.restype = c_int
+    L.zyfa_attn_fwd_fp8_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                                       c_float, vp, vp, vp, vp, c_int, vp, ctypes.c_size_t, vp]
     L.zyfa_quantize_fp8_rows.restype = c_int
     L.zyfa_quantize_fp8_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, c_int, c_int,
                                          c_int, c_int, c_int, c_int, c_int, vp]
@@ -217,12 +225,35 @@ def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard
     return out
 
 
+def _attn_workspace(B: int, S: int, Hq: int, device, split, stream):
+    """(pointer, bytes, tensor) of the split-key-range workspace of an
+    equal-length call: split=True allocates one when the library could split
+    this problem (zyfa_attn_workspace_bytes > 0), a uint8 CUDA tensor is used
+    as given, False gives none (the unsplit call)."""
+    if split is False or split is None:
+        return None, 0, None
+    if isinstance(split, torch.Tensor):
+        if not split.is_cuda or split.dtype != torch.uint8:
+            raise ValueError("workspace must be a uint8 CUDA tensor")
+        return split.data_ptr(), split.numel(), split
+    n = lib().zyfa_attn_workspace_bytes(B, S, Hq)
+    if n == 0:
+        return None, 0, None
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)
+    return ws.data_ptr(), ws.numel(), ws
+
+
 def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: Optional[float] = None,
                   out: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None,
-                  rows: Optional[Tuple[int, int]] = None) -> torch.Tensor:
+                  rows: Optional[Tuple[int, int]] = None, split=False) -> torch.Tensor:
     """Causal attention on bf16 q [B,S,Hq,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv] -> o [B,S,Hq,Dv] bf16.
-    rows=(begin, end): only those output rows (multiples of 256, or end = S)."""
+    rows=(begin, end): only those output rows (multiples of 256, or end = S).
+    split=True (or a uint8 workspace tensor): small problems split each
+    query-tile pair's keys across CTAs (zyfa_attn_fwd_bf16_ws); the result
+    differs from the unsplit call in the last bits."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _require(t, n, torch.bfloat16)
     B, S, Hq, Dqk = q.shape
@@ -232,7 +263,12 @@ def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_sca
     if out is None:
         out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     _require(out, "out", torch.bfloat16)
-    if rows is None:
+    ws_ptr, ws_bytes, _ws = _attn_workspace(B, S, Hq, q.device, split, stream) if rows is None else (None, 0, None)
+    if ws_ptr is not None:
+        _check(lib().zyfa_attn_fwd_bf16_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq,
+                                           Hkv, Dqk, Dv, float(softmax_scale), _strides(q), _strides(k),
+                                           _strides(v), _strides(out), ws_ptr, ws_bytes, _stream_ptr(q, stream)))
+    elif rows is None:
         _check(lib().zyfa_attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, Hq, Hkv,
                                         Dqk, Dv, float(softmax_scale), _strides(q), _strides(k), _strides(v),
                                         _strides(out), _stream_ptr(q, stream)))
@@ -248,9 +284,10 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
                  v8: torch.Tensor, v_scale: torch.Tensor, softmax_scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None,
-                 rows: Optional[Tuple[int, int]] = None, lean_p: bool = False) -> torch.Tensor:
+                 rows: Optional[Tuple[int, int]] = None, lean_p: bool = False, split=False) -> torch.Tensor:
     """Causal attention on per-block e4m3 inputs (uint8 codes + float32 block scales) -> bf16 o.
-    rows=(begin, end): only those output rows (multiples of 256, or end = S)."""
+    rows=(begin, end): only those output rows (multiples of 256, or end = S).
+    split: as attn_fwd_bf16 (zyfa_attn_fwd_fp8_ws)."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
         _require(t, n, torch.uint8)
     for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
@@ -266,7 +303,14 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
     if out is None:
         out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=q8.device)
     _require(out, "out", torch.bfloat16)
-    if rows is None:
+    ws_ptr, ws_bytes, _ws = _attn_workspace(B, S, Hq, q8.device, split, stream) if rows is None else (None, 0, None)
+    if ws_ptr is not None:
+        _check(lib().zyfa_attn_fwd_fp8_ws(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                          v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk,
+                                          Dv, float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
+                                          _strides(out), _fp8_flags(lean_p), ws_ptr, ws_bytes,
+                                          _stream_ptr(q8, stream)))
+    elif rows is None:
         _check(lib().zyfa_attn_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
                                        v8.data_ptr(), v_scale.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, Dqk, Dv,
                                        float(softmax_scale), _strides(q8), _strides(k8), _strides(v8),
@@ -281,13 +325,14 @@ def attn_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_sc
 
 def prefill_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, hadamard: bool = False,
                 softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False):
+                stream: Optional[torch.cuda.Stream] = None, lean_p: bool = False, split=False):
     """The FP8 prefill path: quantise Q and K (optionally rotated) and V in
-    one launch, then FP8 attention. Returns (o, (q8, qs, k8, ks, v8, vs))."""
+    one launch, then FP8 attention (split: as attn_fwd_fp8). Returns
+    (o, (q8, qs, k8, ks, v8, vs))."""
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(q.shape[3])
     (q8, qs), (k8, ks), (v8, vs) = quantize_fp8_qkv(q, k, v, hadamard, stream=stream)
-    o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream, lean_p=lean_p)
+    o = attn_fwd_fp8(q8, qs, k8, ks, v8, vs, softmax_scale, out=out, stream=stream, lean_p=lean_p, split=split)
     return o, (q8, qs, k8, ks, v8, vs)
 
 

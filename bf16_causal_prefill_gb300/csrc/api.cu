@@ -376,10 +376,115 @@ static int groups_in_flight(int S, int Dqk, int Dv, int elt) {
   return 8 * group_bytes > kHalfL2Bytes ? 4 : 8;
 }
 
+// Few query-tile pairs (fewer than SMs, e.g. a long sequence with few
+// heads): the longest pair's chain of key blocks sets the time while most
+// SMs idle. With a caller workspace the key blocks of every pair can be
+// split into chunks of C blocks (C even, at most kMaxKeyChunks chunks per
+// query tile) that run on separate CTAs, a second kernel combining the
+// chunks' partial rows. The host picks C with a cost model in units of one
+// key block of a pair (~1.25 us on a GB300): the kernel's static schedule
+// simulated (unit u on CTA u mod grid, pairs longest first, kUnitCost per
+// unit for its start and its partial-row stores) plus the combine, which
+// moves every partial row twice (written, then read: kCombineBytesPerBlock
+// per key block of time) after a second launch (kCombineLaunch). It splits
+// only where that comes to less than 85% of the unsplit schedule with
+// kMinGain blocks to spare. The constants were fitted to GB300 timings of
+// split and unsplit calls (FP8, one and two heads, 4K to 32K tokens): one
+// head at 4K, 8K, 16K tokens ran 1.8x, 2.1x, 1.7x faster split, two heads
+// at 16K 7% slower (left unsplit by the model), the 1K-token 2-head
+// workload unsplit.
+constexpr int kMaxKeyChunks = 8;
+constexpr int kUnitCost = 4;
+constexpr int kMinGain = 4;
+constexpr double kCombineBytesPerBlock = 2.5e6;
+constexpr int kCombineLaunch = 5;
+
+static int pair_key_blocks(int t, int nq) { return (2 * t + 1 < nq) ? 2 * t + 2 : 2 * t + 1; }
+
+// Largest per-CTA cost of the static schedule with chunks of C key blocks
+// (C = 0: one unit per pair), and the unit count.
+static long long schedule_cost(int B, int Hq, int nq, int sms, int C, long long* units) {
+  const int pairs = (nq + 1) / 2;
+  const long long bh = static_cast<long long>(B) * Hq;
+  long long n = 0;
+  for (int t = 0; t < pairs; ++t) n += C ? (pair_key_blocks(t, nq) + C - 1) / C : 1;
+  n *= bh;
+  *units = n;
+  const long long grid = std::min<long long>(n, sms);
+  std::vector<long long> load(static_cast<size_t>(std::max<long long>(grid, 1)), 0);
+  long long u = 0;
+  for (int t = pairs - 1; t >= 0; --t) {
+    const int nk = pair_key_blocks(t, nq);
+    const int nch = C ? (nk + C - 1) / C : 1;
+    for (int c = 0; c < nch; ++c) {
+      const int len = C ? std::min(C, nk - c * C) : nk;
+      for (long long i = 0; i < bh; ++i, ++u) load[static_cast<size_t>(u % grid)] += len + kUnitCost;
+    }
+  }
+  long long cost = *std::max_element(load.begin(), load.end());
+  if (C) {
+    // partial rows: both query tiles of pair t write one per chunk of its key blocks
+    double rows = 0;
+    for (int t = 0; t < pairs; ++t) rows += (2 * t + 1 < nq ? 2 : 1) * 128.0 * ((pair_key_blocks(t, nq) + C - 1) / C);
+    rows *= static_cast<double>(bh);
+    cost += kCombineLaunch + static_cast<long long>(2.0 * rows * (128 * 4 + 8) / kCombineBytesPerBlock);
+  }
+  return cost;
+}
+
+static int min_split_tiles(int nq) {
+  const int c = (nq + kMaxKeyChunks - 1) / kMaxKeyChunks;
+  return std::max(2, (c + 1) & ~1);
+}
+
+// C for this problem on `sms` SMs, or 0 (no split); units: the split unit count.
+static int prefill_split_tiles(int B, int S, int Hq, int sms, long long* units) {
+  if (B < 1 || S < 1 || Hq < 1 || sms < 1) return 0;
+  const int nq = (S + 127) / 128, pairs = (nq + 1) / 2;
+  if (static_cast<long long>(B) * Hq * pairs >= sms) return 0;
+  long long n0;
+  const long long plain = schedule_cost(B, Hq, nq, sms, 0, &n0);
+  long long best = plain;
+  int best_c = 0, prev = 0;
+  // candidates: the smallest even C giving the longest query tile k chunks
+  for (int k = kMaxKeyChunks; k >= 2; --k) {
+    const int c = (nq + k - 1) / k;
+    const int C = std::max(min_split_tiles(nq), (c + 1) & ~1);
+    if (C >= nq || C == prev) continue;
+    prev = C;
+    long long n;
+    const long long cost = schedule_cost(B, Hq, nq, sms, C, &n) + kMinGain;
+    if (cost < best) { best = cost; best_c = C; }
+  }
+  if (best_c && 100 * best >= 85 * plain) best_c = 0;
+  if (best_c) schedule_cost(B, Hq, nq, sms, best_c, units);
+  return best_c;
+}
+
+// Partial rows of a split call: at most kMaxKeyChunks chunks x B x 128 tiles x
+// Hq, for problems of fewer than kMaxSmsForPrefillSplit pairs and more than
+// two query tiles (whether the call splits depends on the GPU's SM count);
+// 0 otherwise.
+constexpr int kMaxSmsForPrefillSplit = 256;
+static size_t prefill_partial_rows(int B, int S, int Hq) {
+  if (B < 1 || S < 1 || Hq < 1) return 0;
+  const int nq = (S + 127) / 128, pairs = (nq + 1) / 2;
+  if (nq <= 2 || static_cast<long long>(B) * Hq * pairs >= kMaxSmsForPrefillSplit) return 0;
+  const int chunks = (nq + min_split_tiles(nq) - 1) / min_split_tiles(nq);
+  return static_cast<size_t>(chunks) * B * (static_cast<size_t>(nq) * 128) * Hq;
+}
+
+static size_t prefill_ws_bytes(int B, int S, int Hq) {
+  // per partial row: 128 fp32 of O, then (m, l) after the O block
+  const size_t rows = prefill_partial_rows(B, S, Hq);
+  return rows ? ((rows * 128 * 4 + 255) & ~size_t(255)) + rows * 2 * 4 : 0;
+}
+
 static int attn_common(bool fp8, int lean, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[3], const int64_t ks[3], const int64_t vs[3],
-                       const int64_t os[3], int row_begin, int row_end, void* stream) {
+                       const int64_t os[3], int row_begin, int row_end, void* stream, void* workspace = nullptr,
+                       size_t workspace_bytes = 0) {
   AttnCommon c{B, S, Hq, Hkv, Dqk, Dv, softmax_scale};
   const int elt = fp8 ? 1 : 2;
   if (int r = validate_attn(c, q, k, v, o, 16 / elt, qs, ks, vs, os)) return r;
@@ -415,10 +520,50 @@ static int attn_common(bool fp8, int lean, const void* q, const float* qsc, cons
   a.pair_lo = row_begin / 256;
   a.pair_hi = (row_end + 255) / 256;
   a.groups_in_flight = groups_in_flight(S, Dqk, Dv, elt);
+  long long split_units = 0;
+  const int split = (workspace && row_begin == 0 && row_end == S)
+                        ? prefill_split_tiles(B, S, Hq, d->sm_count, &split_units) : 0;
+  if (split) {
+    if (!aligned(workspace, 256)) return fail(ZYFA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < prefill_ws_bytes(B, S, Hq))
+      return fail(ZYFA_ERR_INVALID_ARG, "workspace of %zu bytes is below zyfa_attn_workspace_bytes = %zu",
+                  workspace_bytes, prefill_ws_bytes(B, S, Hq));
+    const size_t rows = prefill_partial_rows(B, S, Hq);
+    a.split_tiles = split;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * 128 * 4 + 255) & ~size_t(255)));
+    cudaError_t e = fp8 ? zyfa::launch_attn_fp8_split(tq, tk, tv, a, split_units, static_cast<cudaStream_t>(stream))
+                        : zyfa::launch_attn_bf16_split(tq, tk, tv, a, split_units, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
+    e = zyfa::launch_prefill_combine(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "prefill_combine launch");
+    return ZYFA_OK;
+  }
   cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
                       : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
   return ZYFA_OK;
+}
+
+size_t zyfa_attn_workspace_bytes(int B, int S, int Hq) { return prefill_ws_bytes(B, S, Hq); }
+
+int zyfa_attn_fwd_bf16_ws(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                          int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
+                          const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_common(false, 0, q, nullptr, k, nullptr, v, nullptr, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale, q_strides,
+                     k_strides, v_strides, o_strides, 0, S, stream, workspace, workspace_bytes);
+}
+
+int zyfa_attn_fwd_fp8_ws(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                         const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                         int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                         const int64_t v_strides[3], const int64_t o_strides[3], int flags, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  const int lean = fp8_flags_lean(flags);
+  if (lean < 0) return lean_flags_error(flags);
+  return attn_common(true, lean, q8, q_scale, k8, k_scale, v8, v_scale, o, B, S, Hq, Hkv, Dqk, Dv, softmax_scale,
+                     q_strides, k_strides, v_strides, o_strides, 0, S, stream, workspace, workspace_bytes);
 }
 
 int zyfa_attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv, int Dqk,

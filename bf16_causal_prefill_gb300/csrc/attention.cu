@@ -176,22 +176,66 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int Hq, int Hkv, int n
 // (decode_unit). Packed variable lengths: the host-built level table.
 struct NoTable {};
 
-// DECODE: the kernel instantiation runs decode steps (one query token per
-// sequence); prefill instantiations compile none of that code.
-template <bool VARLEN, bool DECODE = false>
+// PART: the kernel instantiation's units write partial rows (unnormalised
+// O and the row's offset or maximum and sum) that a second kernel combines.
+// Packed batches: decode steps (one query token per sequence, key ranges
+// split across units); prefill instantiations compile none of that code.
+// Equal lengths: query-tile pairs whose key blocks are split into chunks of
+// split_tiles blocks (small grids, where pairs alone leave SMs idle).
+template <bool VARLEN, bool PART = false>
 struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
   int B, Hq, Hkv, S, n_qtiles, pair_lo, pair_hi;
   int groups_in_flight;    // equal lengths: KV groups per super-group of the work order
-  bool one_token;          // decode step: one query token per sequence, its heads as tile rows (DECODE only)
-  __device__ __forceinline__ bool step() const { return DECODE && one_token; }
-  int split_tiles;         // decode step: nonzero when key ranges are split (per-sequence split counts in tab)
+  bool one_token;          // decode step: one query token per sequence, its heads as tile rows (PART only)
+  __device__ __forceinline__ bool step() const { return VARLEN && PART && one_token; }
+  int split_tiles;         // nonzero when key ranges are split (decode: per-sequence split counts in tab;
+                           // equal lengths: key blocks per chunk, even)
+  // Equal lengths with split key ranges: pairs are taken longest first, each
+  // as ceil(key blocks / split_tiles) chunks, each chunk for every (batch,
+  // query head). Tile A of a chunk always has a key block: split_tiles is
+  // even and so is tile B's key count.
+  __device__ __forceinline__ int pair_chunks(int t) const {
+    const int nk = (2 * t + 1 < n_qtiles) ? 2 * t + 2 : 2 * t + 1;
+    return (nk + split_tiles - 1) / split_tiles;
+  }
+  __device__ __forceinline__ int split_units() const {
+    int n = 0;
+    for (int t = pair_lo; t < pair_hi; ++t) n += pair_chunks(t);
+    return n * B * Hq;
+  }
+  __device__ __forceinline__ Unit decode_split(int u) const {
+    int rem = u, t = pair_hi - 1, nch = 0;
+    for (; t > pair_lo; --t) {
+      nch = pair_chunks(t) * B * Hq;
+      if (rem < nch) break;
+      rem -= nch;
+    }
+    const int c = rem / (B * Hq), bh = rem - c * (B * Hq);
+    Unit w;
+    w.b = bh / Hq;
+    w.hq = bh - w.b * Hq;
+    w.t = t;
+    w.has_b = (2 * t + 1) < n_qtiles;
+    w.j0 = c * split_tiles;
+    w.n_a = min(split_tiles, 2 * t + 1 - w.j0);
+    w.n_b = w.has_b ? min(split_tiles, 2 * t + 2 - w.j0) : 0;
+    w.n_kv = w.has_b ? w.n_b : w.n_a;
+    w.c0 = 0;
+    w.dlt = 0;
+    w.part = c;
+    w.row0 = 0;
+    w.len = S;
+    w.sidx = w.b;
+    return w;
+  }
   __device__ __forceinline__ int n_tasks() const {
     return split_tiles ? tab->level_start[tab->n_seqs] : tab->n_seqs * Hkv;
   }
   __device__ __forceinline__ int n_units() const {
     if constexpr (VARLEN) return step() ? (n_tasks() + 1) / 2 : tab->level_start[tab->n_levels];
+    else if constexpr (PART) return split_units();
     else return B * Hq * (pair_hi - pair_lo);
   }
   // Decode step: task i = (sequence of rank i / Hkv, KV head i % Hkv), the
@@ -278,6 +322,8 @@ struct Sched {
       w.n_b = min(w.c0 + 2 * w.t + 2 + ext, nk);
       w.n_kv = w.has_b ? w.n_b : w.n_a;
       return w;
+    } else if constexpr (PART) {
+      return decode_split(u);
     } else {
       Unit w = decode_unit(u, B, Hq, Hkv, n_qtiles, pair_lo, pair_hi, groups_in_flight);
       w.len = S;
@@ -351,9 +397,9 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 // and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
-template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE, bool DECODE>
+template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE, bool PART>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
-                            const AttnArgs& a, const Sched<VARLEN, DECODE>& sc, bool leader) {
+                            const AttnArgs& a, const Sched<VARLEN, PART>& sc, bool leader) {
   using C = Cfg<DQK, FP8>;
   constexpr bool kIsK = (STREAM == kStreamQK);
   constexpr int kStages = kIsK ? C::kNK : C::kNV;
@@ -453,7 +499,8 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
     int pages = 0;   // paged K/V: block-table entries j & ~31 .. + 31, one per lane
     for (int j = 0; j < w.n_kv; ++j) {
       // Key block j: tokens row0 + 128 j of batch b, or all 128 tokens of its page.
-      int kv_row = w.row0 + j * 128, kv_b = w.b;
+      // (equal lengths with split key ranges: the chunk starts at block j0)
+      int kv_row = w.row0 + ((!VARLEN && PART) ? w.j0 + j : j) * 128, kv_b = w.b;
       if constexpr (VARLEN) {
         if (a.block_table) {
           if ((j & 31) == 0) {
@@ -543,8 +590,8 @@ __device__ __forceinline__ void issue_pv(const OperandDescs& od, uint32_t tmem_p
 // The whole warp runs the schedule (waits, stage and phase bookkeeping,
 // descriptors: all warp-uniform); one elected lane issues tcgen05.mma and
 // tcgen05.commit, so a commit tracks exactly the MMAs of that lane.
-template <int DQK, bool FP8, bool VARLEN, bool DECODE>
-__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, DECODE>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool PART>
+__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART>& sc,
                          bool leader) {
   using C = Cfg<DQK, FP8>;
   const int n_units = sc.n_units();
@@ -995,8 +1042,8 @@ __device__ __forceinline__ void slice_probs(uint32_t tS, uint32_t tO, int cpy, b
   if (moved) rescale_o_row(tO, rho);
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool DECODE>
-__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, DECODE>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART>
+__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART>& sc,
                              int warp, int lane) {
   const int n_units = sc.n_units();
   const int nblk = a.scale_blocks;
@@ -1045,7 +1092,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
     // per sequence block, or per page (block table read 32 entries at a
     // time, one per lane).
     auto kv_index = [&](int jj) -> int64_t {
-      int64_t kv_i = kv_scale_row + jj;
+      int64_t kv_i = kv_scale_row + jj + ((!VARLEN && PART) ? w.j0 : 0);
       if constexpr (VARLEN) {
         if (a.block_table) {
           if ((jj & 31) == 0) {
@@ -1107,6 +1154,9 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
           diag = (ja == ((w.len - 1) >> 7));
           lim = w.len - 1 - 128 * ja;
         }
+      } else if constexpr (PART) {
+        diag = (w.j0 + j == qt);   // the diagonal block ends the chunk that holds it
+        lim = r;
       } else {
         diag = (j == n - 1);
         lim = r;
@@ -1235,6 +1285,28 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
         continue;
       }
     }
+    if constexpr (!VARLEN && PART) {
+      // split key range: unnormalised O and (m, l) of chunk w.part, row
+      // ((part * B + b) * Spad + query row) * Hq + query head, Spad = 128 x
+      // query tiles; combined by prefill_combine_kernel
+      const int q_row = qt * 128 + r;
+      const int64_t prow =
+          ((static_cast<int64_t>(w.part) * a.B + w.b) * (sc.n_qtiles * 128) + q_row) * a.Hq + w.hq;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        __syncwarp();
+        tmem_ld32(tO + 32 * c, o);
+        if (q_row < a.S) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(u2f(o[4 * e]), u2f(o[4 * e + 1]), u2f(o[4 * e + 2]), u2f(o[4 * e + 3]));
+        }
+      }
+      if (q_row < a.S) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m, l);
+      continue;
+    }
     const float inv = 1.f / l;
     const int q_row = qt * 128 + r;
     __nv_bfloat16* orow = out + w.b * a.o_sb + static_cast<int64_t>(w.row0 + q_row) * a.o_ss + w.hq * a.o_sh;
@@ -1264,7 +1336,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool DECODE>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
@@ -1276,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Sched<VARLEN, DECODE> sc;
+  Sched<VARLEN, PART> sc;
   // The unit table comes by value (built on the host) or, when the sequence
   // offsets live on the device, from global memory (built by a kernel).
   sc.tab = tab_global ? tab_global : &tab;
@@ -1323,16 +1395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE, DECODE>(sm, &tm_q, &tm_k, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE, PART>(sm, &tm_q, &tm_k, a, sc, leader);
     } else if (warp == kLoadWarpV) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE, DECODE>(sm, &tm_q, &tm_v, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE, PART>(sm, &tm_q, &tm_v, a, sc, leader);
     } else if (warp == kMmaWarp) {
       mma_role(sm, tmem, a, sc, leader);
     }
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE, DECODE>(sm, tmem, a, sc, warp, lane);
+    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE, PART>(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -1343,12 +1415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false, bool DECODE = SLICE>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false, bool PART = SLICE>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                    const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream,
                    const typename Sched<VARLEN>::Table* tab_global = nullptr) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE, DECODE>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE, PART>;
   // The shared-memory opt-in is per function and device: set it once.
   static bool opted_in[64] = {};
   int dev = 0;
@@ -1388,6 +1460,87 @@ cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
   return cudaErrorInvalidValue;
 }
 
+// Equal lengths with split key ranges (a.split_tiles key blocks per chunk,
+// even): the PART instantiations write partial rows, prefill_combine_kernel
+// merges them. n_units = (batch, query head) x the chunks of every pair.
+cudaError_t launch_attn_bf16_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const AttnArgs& a, long long n_units, cudaStream_t stream) {
+  const NoTable none{};
+  if (a.Dqk == 128) return launch<128, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n_units, stream);
+  if (a.Dqk == 192) return launch<192, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n_units, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fp8_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                  const AttnArgs& a, long long n_units, cudaStream_t stream) {
+  const NoTable none{};
+  if (a.Dqk == 128 && a.lean_p)
+    return launch<128, true, false, true, false, true>(tm_q, tm_k, tm_v, a, none, n_units, stream);
+  if (a.Dqk == 128) return launch<128, true, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n_units, stream);
+  if (a.Dqk == 192) return launch<192, true, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n_units, stream);
+  return cudaErrorInvalidValue;
+}
+
+// Equal lengths with split key ranges: out = sum_c O_c 2^(m_c - M) /
+// sum_c l_c 2^(m_c - M), M = max_c m_c, over the key chunks c of the row's
+// query-tile pair. One warp per (batch, row, query head), four output
+// columns per lane (16-byte loads of the partial rows, 8-byte stores), eight
+// rows per 256-thread block. While the device status word records a
+// timed-out wait, out is left untouched.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ part_o,
+                                                              const float2* __restrict__ part_ml, int B, int S,
+                                                              int Hq, int n_qtiles, int split_tiles,
+                                                              __nv_bfloat16* __restrict__ out, int64_t o_sb,
+                                                              int64_t o_ss, int64_t o_sh,
+                                                              const unsigned int* status) {
+  if (*reinterpret_cast<const volatile unsigned int*>(status) &
+      (kStatusLoaderTimeout | kStatusMmaTimeout | kStatusSoftmaxTimeout))
+    return;
+  const int lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (idx >= static_cast<int64_t>(B) * S * Hq) return;
+  const int h = static_cast<int>(idx % Hq);
+  const int row = static_cast<int>((idx / Hq) % S);
+  const int b = static_cast<int>(idx / (static_cast<int64_t>(Hq) * S));
+  const int t = (row >> 7) >> 1;
+  const int nk = (2 * t + 1 < n_qtiles) ? 2 * t + 2 : 2 * t + 1;
+  const int cnt = (nk + split_tiles - 1) / split_tiles;
+  const int64_t spad = static_cast<int64_t>(n_qtiles) * 128;
+  auto prow = [&](int c) { return ((static_cast<int64_t>(c) * B + b) * spad + row) * Hq + h; };
+  float mx = -INFINITY;
+  for (int c = 0; c < cnt; ++c) mx = fmaxf(mx, part_ml[prow(c)].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int c = 0; c < cnt; ++c) {
+    const float2 ml = part_ml[prow(c)];
+    const float wgt = exp2f(ml.x - mx);
+    den = fmaf(ml.y, wgt, den);
+    const float4 o = reinterpret_cast<const float4*>(part_o + prow(c) * 128)[lane];
+    acc.x = fmaf(o.x, wgt, acc.x);
+    acc.y = fmaf(o.y, wgt, acc.y);
+    acc.z = fmaf(o.z, wgt, acc.z);
+    acc.w = fmaf(o.w, wgt, acc.w);
+  }
+  const float inv = 1.f / den;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pkd;
+  pkd.x = *reinterpret_cast<uint32_t*>(&lo);
+  pkd.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + b * o_sb + static_cast<int64_t>(row) * o_ss + static_cast<int64_t>(h) * o_sh +
+                            4 * lane) = pkd;
+}
+
+cudaError_t launch_prefill_combine(const AttnArgs& a, cudaStream_t stream) {
+  const int n_qtiles = (a.S + 127) / 128;
+  const long long rows = static_cast<long long>(a.B) * a.S * a.Hq;
+  if (rows == 0) return cudaSuccess;
+  prefill_combine_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      a.part_o, reinterpret_cast<const float2*>(a.part_ml), a.B, a.S, a.Hq, n_qtiles, a.split_tiles,
+      static_cast<__nv_bfloat16*>(a.o), a.o_sb, a.o_ss, a.o_sh, a.status);
+  return cudaGetLastError();
+}
+
 long long table_units(const AttnArgs& a, const SeqTable& tab) {
   if (!a.one_token) return tab.level_start[tab.n_levels];
   const long long tasks = a.split_tiles ? tab.level_start[tab.n_seqs] : static_cast<long long>(tab.n_seqs) * a.Hkv;
@@ -1422,7 +1575,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float* __rest
   out[static_cast<int64_t>(i) * o_ss + static_cast<int64_t>(h) * o_sh + threadIdx.x] = __float2bfloat16_rn(acc / den);
 }
 
-// Decode steps (a.one_token) run their own instantiations (DECODE), so the
+// Decode steps (a.one_token) run their own instantiations (PART), so the
 // packed and paged prefill kernels carry none of the one-token code.
 cudaError_t launch_attn_bf16_varlen(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     const AttnArgs& a, const SeqTable& tab, cudaStream_t stream) {

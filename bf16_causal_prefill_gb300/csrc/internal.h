@@ -128,6 +128,17 @@ struct AttnArgs {
   int replicate;
 };
 
+// Equal lengths with split key ranges (a.split_tiles > 0, even): units are
+// (batch, query head, query-tile pair, chunk of split_tiles key blocks); each
+// writes unnormalised O to part_o and (m, l) to part_ml at row ((chunk * B +
+// b) * Spad + query row) * Hq + head, Spad = 128 * ceil(S / 128), and
+// launch_prefill_combine writes o. n_units counts the chunks of all pairs.
+cudaError_t launch_attn_bf16_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const AttnArgs& a, long long n_units, cudaStream_t stream);
+cudaError_t launch_attn_fp8_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                  const AttnArgs& a, long long n_units, cudaStream_t stream);
+cudaError_t launch_prefill_combine(const AttnArgs& a, cudaStream_t stream);
+
 // Partial rows of each sequence (caller's order) for decode_combine.
 struct CombineTable {
   int base[kMaxVarlenSeqs];

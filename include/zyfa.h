@@ -8,10 +8,12 @@
  * 128-point Hadamard rotation of Q and K before quantisation.
  *
  * Entry points: the quantiser and the two attention calls on [B, S, H, D]
- * batches (plus query-row ranges and a prefill from page-locked host
- * memory); the same on packed variable-length batches (offsets on the host
- * or on the device); packed queries that continue cached sequences over a
- * paged K/V cache; and a decode step over that cache.
+ * batches (plus query-row ranges, a caller workspace that lets calls with
+ * few query tiles split their key ranges across CTAs, and a prefill from
+ * page-locked host memory); the same on packed variable-length batches
+ * (offsets on the host or on the device); packed queries that continue
+ * cached sequences over a paged K/V cache; and a decode step over that
+ * cache.
  *
  * Sources of the operations (page title, section):
  *   - "ZYFA: Fast and Accurate FP8 Attention on AMD MI355X": "Introduction"
@@ -190,6 +192,42 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
                       const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
                       int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
                       const int64_t v_strides[3], const int64_t o_strides[3], int flags, void* stream);
+
+/*
+ * The two calls above with a caller workspace, for calls with fewer pairs of
+ * 128-row query tiles (B * Hq * ceil(S / 256)) than SMs, such as long
+ * sequences with few heads ("ZYFA ...", "Introduction": the same causal
+ * attention). There the longest pair's chain of key blocks sets the time
+ * while most SMs idle, so each pair's key blocks may be split into chunks of
+ * C blocks (C even, at most 8 chunks per query tile) run by separate CTAs:
+ * every chunk writes its rows' unnormalised output with the row's offset (or
+ * running maximum) and rounded sum to the workspace, and a second kernel
+ * combines the chunks, o = sum_c O_c 2^(m_c - M) / sum_c l_c 2^(m_c - M). The
+ * host picks C from a model of the kernel's static schedule and splits only
+ * where that model predicts a clear gain; otherwise, or with workspace ==
+ * NULL, the call is exactly zyfa_attn_fwd_bf16 / _fp8 (same bytes). A split
+ * call rounds differently in the last bits (per-chunk offsets and sums); the
+ * row-range and host-memory forms below reproduce the unsplit call's bytes.
+ *
+ * workspace       : device memory, 256-byte aligned, owned by the caller and
+ *                   not used by anything else until the call's work is done;
+ *                   at least zyfa_attn_workspace_bytes(B, S, Hq) bytes
+ *                   (smaller: ZYFA_ERR_INVALID_ARG when the call splits).
+ * workspace_bytes : its size.
+ * zyfa_attn_workspace_bytes: 0 for problems no GPU would split (256 or more
+ *                   query-tile pairs, or S <= 256).
+ * Other arguments and errors as the calls above.
+ */
+size_t zyfa_attn_workspace_bytes(int B, int S, int Hq);
+int zyfa_attn_fwd_bf16_ws(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
+                          int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
+                          const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],
+                          void* workspace, size_t workspace_bytes, void* stream);
+int zyfa_attn_fwd_fp8_ws(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                         const void* v8, const float* v_scale, void* o, int B, int S, int Hq, int Hkv, int Dqk,
+                         int Dv, float softmax_scale, const int64_t q_strides[3], const int64_t k_strides[3],
+                         const int64_t v_strides[3], const int64_t o_strides[3], int flags, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * Row-range ("chunked prefill") forms of the two calls above: only output rows

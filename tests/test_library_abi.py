@@ -325,3 +325,28 @@ def test_noalloc_call_refuses_what_its_static_table_cannot_hold(L):
     assert call(4, 300000) == 2
     assert b"static scratch" in L.zyfa_last_error_message()
 
+
+
+def test_attn_workspace_size(L):
+    """Split key ranges apply to problems of fewer than 256 query-tile pairs
+    with more than two query tiles (at most 8 chunks per query tile); the
+    size grows with the problem."""
+    f = L.zyfa_attn_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 3
+    assert f(1, 256, 8) == 0                  # one pair of at most two key blocks: nothing to split
+    assert f(1, 32768, 32) == 0               # 4096 pairs fill the GPU
+    assert f(0, 1024, 2) == 0 and f(1, 0, 2) == 0
+    small, big = f(1, 1024, 2), f(1, 16384, 1)
+    # 1K, 2 heads: 4 chunks (2 key blocks each) x 1024 rows x 2 heads partial
+    # rows of 128 fp32 + (m, l)
+    assert small == 4 * 1024 * 2 * 128 * 4 + 4 * 1024 * 2 * 8
+    # 16K, 1 head: 8 chunks of 16 key blocks
+    assert big == 8 * 16384 * 128 * 4 + 8 * 16384 * 8
+
+
+def test_attn_ws_calls_refuse_bad_arguments_before_launch(L):
+    s3 = (ctypes.c_int64 * 3)(128 * 2, 128, 128)
+    rc = L.zyfa_attn_fwd_bf16_ws(None, 16, 16, 16, 1, 128, 2, 2, 128, 128, ctypes.c_float(0.1), s3, s3, s3, s3,
+                                 None, 0, None)
+    assert rc == 1   # ZYFA_ERR_INVALID_ARG: null q
