@@ -43,11 +43,14 @@ METRIC = "causal prefill attn TFLOP/s (FP8, BF16) at 32K tokens; % of GB300 dens
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor-core rate ratio on GB300
-# Per-SM issue rates of the softmax's two special-function steps, measured on
-# a GB300 with a register-only microbenchmark (4 warps per sub-partition):
-# ex2.approx.ftz.f32 results and cvt.rn.satfinite.e4m3x2.f32 elements per clock.
+# Per-SM rates of the softmax's two special-function steps, measured on a
+# GB300 with register-only microbenchmarks: ex2.approx.ftz.f32 results per
+# clock (30.5 measured with 8 to 32 warps per SM, 32 the unit's rate), and
+# cvt.rn.satfinite.e4m3x2.f32 converted elements per clock (94.5 to 98.5
+# with 16 warps per SM, inputs perturbed each iteration, the folding of the
+# results subtracted).
 EX2_PER_CLK_SM = 32.0
-E4M3_CVT_PER_CLK_SM = 69.0
+E4M3_CVT_PER_CLK_SM = 98.5
 L2_FLUSH_BYTES = 256 << 20
 
 
