@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "../../include/zyfa.h"
@@ -480,6 +481,61 @@ static size_t prefill_ws_bytes(int B, int S, int Hq) {
   return rows ? ((rows * 128 * 4 + 255) & ~size_t(255)) + rows * 2 * 4 : 0;
 }
 
+// Multi-wave equal-length calls: CTA c of the persistent kernel would run
+// units c, c + grid, ... (round robin); with query-tile pairs of very
+// different lengths that leaves the busiest CTA with several percent more
+// work than the average (32K GQA: 3.5%; 8K batch 2 and the activation-like
+// 16K: about 10%, by the model below). The host instead hands the units out
+// in the kernel's order, each to the CTA with the least work so far (what a
+// work queue would do, without one): cost = the pair's key blocks plus
+// kListUnitCost for the unit's start. The list goes to the kernel as a
+// parameter, cached for the last shape.
+constexpr int kListUnitCost = 2;
+
+static int unit_key_blocks(int u, const zyfa::AttnArgs& a, int n_qtiles) {
+  const int n_pairs = a.pair_hi - a.pair_lo, G = a.Hq / a.Hkv, n_groups = a.B * a.Hkv;
+  const int gif = std::max(1, a.groups_in_flight);
+  const int per_sg = gif * G * n_pairs;
+  const int sg = u / per_sg, r = u - sg * per_sg;
+  const int gs_here = std::min(gif, n_groups - sg * gif);
+  const int t = a.pair_hi - 1 - r / (gs_here * G);
+  return (2 * t + 1 < n_qtiles) ? 2 * t + 2 : 2 * t + 1;
+}
+
+static const zyfa::UnitList* unit_list(const zyfa::AttnArgs& a) {
+  const long long n = static_cast<long long>(a.B) * a.Hq * (a.pair_hi - a.pair_lo);
+  const int G = a.num_sms;
+  if (n <= G || n > zyfa::kMaxListUnits || G > zyfa::kMaxListCtas) return nullptr;
+  // Row-range calls (the host pipeline's pieces) keep the round robin: their
+  // pairs are of similar length, and consecutive pieces on two streams fill
+  // each other's idle SMs (the end-to-end prefill measured 0.2 ms slower
+  // with per-piece lists).
+  if (a.pair_lo != 0 || a.pair_hi != (a.S + 255) / 256) return nullptr;
+  static thread_local zyfa::UnitList list;
+  static thread_local long long key[8] = {-1};
+  const long long k[8] = {a.B, a.S, a.Hq, a.Hkv, a.pair_lo, a.pair_hi, a.groups_in_flight, G};
+  if (std::equal(k, k + 8, key)) return &list;
+  const int n_qtiles = (a.S + 127) / 128;
+  std::vector<int> owner(static_cast<size_t>(n));
+  std::vector<int> count(G, 0);
+  using Load = std::pair<long long, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < G; ++c) heap.push({0, c});
+  for (int u = 0; u < n; ++u) {
+    const Load top = heap.top();
+    heap.pop();
+    owner[u] = top.second;
+    ++count[top.second];
+    heap.push({top.first + unit_key_blocks(u, a, n_qtiles) + kListUnitCost, top.second});
+  }
+  list.start[0] = 0;
+  for (int c = 0; c < G; ++c) list.start[c + 1] = static_cast<uint16_t>(list.start[c] + count[c]);
+  std::vector<int> fill(list.start, list.start + G);
+  for (int u = 0; u < n; ++u) list.unit[fill[owner[u]]++] = static_cast<uint16_t>(u);
+  std::copy(k, k + 8, key);
+  return &list;
+}
+
 static int attn_common(bool fp8, int lean, const void* q, const float* qsc, const void* k, const float* ksc, const void* v,
                        const float* vsc, void* o, int B, int S, int Hq, int Hkv, int Dqk, int Dv,
                        float softmax_scale, const int64_t qs[3], const int64_t ks[3], const int64_t vs[3],
@@ -539,8 +595,9 @@ static int attn_common(bool fp8, int lean, const void* q, const float* qsc, cons
     if (e != cudaSuccess) return fail_cuda(e, "prefill_combine launch");
     return ZYFA_OK;
   }
-  cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
-                      : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
+  const zyfa::UnitList* list = unit_list(a);
+  cudaError_t e = fp8 ? zyfa::launch_attn_fp8(tq, tk, tv, a, static_cast<cudaStream_t>(stream), list)
+                      : zyfa::launch_attn_bf16(tq, tk, tv, a, static_cast<cudaStream_t>(stream), list);
   if (e != cudaSuccess) return fail_cuda(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd_bf16 launch");
   return ZYFA_OK;
 }
@@ -912,8 +969,11 @@ static int attn_decode(bool fp8, int lean, const void* q, const float* qsc, cons
   CUtensorMap tq, tk, tv;
   int r;
   // q as rows of (token, head): the group of a KV head is consecutive rows
-  // from its first head; 32-row boxes when the rows are replicated
-  const bool replicate = workspace != nullptr && Hq / Hkv <= 32;
+  // from its first head; 32-row boxes when the rows are replicated.
+  // Replicated rows need at least 16 (token, KV head) tasks to pay: with one
+  // 32K-token sequence and 8 KV heads they ran 35.9 us (FP8) against 29.8
+  // with full rows, while two sequences and more gain from them.
+  const bool replicate = workspace != nullptr && Hq / Hkv <= 32 && static_cast<int64_t>(N) * Hkv >= 16;
   if ((r = make_map(&tq, q, dt, elt, Dqk, 1, static_cast<int>(rows), 1, q3, "q", replicate ? 32 : 128)) ||
       (r = make_map(&tk, kc, dt, elt, Dqk, Hkv, 128, num_pages, kcs, "k_cache")) ||
       (r = make_map(&tv, vc, dt, elt, Dv, Hkv, 128, num_pages, vcs, "v_cache")))

@@ -182,7 +182,7 @@ struct NoTable {};
 // split across units); prefill instantiations compile none of that code.
 // Equal lengths: query-tile pairs whose key blocks are split into chunks of
 // split_tiles blocks (small grids, where pairs alone leave SMs idle).
-template <bool VARLEN, bool PART = false>
+template <bool VARLEN, bool PART = false, bool LIST = false>
 struct Sched {
   using Table = typename std::conditional<VARLEN, SeqTable, NoTable>::type;
   const Table* tab;
@@ -190,6 +190,23 @@ struct Sched {
   int groups_in_flight;    // equal lengths: KV groups per super-group of the work order
   bool one_token;          // decode step: one query token per sequence, its heads as tile rows (PART only)
   __device__ __forceinline__ bool step() const { return VARLEN && PART && one_token; }
+  // This CTA's units: LIST, the host's list (equal lengths, more than one
+  // wave); else units blockIdx.x, blockIdx.x + gridDim.x, ... below nu.
+  // Walked as u = first(); u >= 0; u = next(++i, u).
+  const UnitList* list;
+  int nu;                  // n_units(), computed once
+  __device__ __forceinline__ int first() const {
+    if constexpr (LIST) return list->start[blockIdx.x + 1] > list->start[blockIdx.x] ? list->unit[list->start[blockIdx.x]] : -1;
+    else return static_cast<int>(blockIdx.x) < nu ? static_cast<int>(blockIdx.x) : -1;
+  }
+  __device__ __forceinline__ int next(int i, int u) const {
+    if constexpr (LIST) {
+      const int b = list->start[blockIdx.x];
+      return b + i < list->start[blockIdx.x + 1] ? list->unit[b + i] : -1;
+    } else {
+      return u + static_cast<int>(gridDim.x) < nu ? u + static_cast<int>(gridDim.x) : -1;
+    }
+  }
   int split_tiles;         // nonzero when key ranges are split (decode: per-sequence split counts in tab;
                            // equal lengths: key blocks per chunk, even)
   // Equal lengths with split key ranges: pairs are taken longest first, each
@@ -397,14 +414,13 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
 // and the expect-tx arrivals.
 enum LoadStream { kStreamQK = 0, kStreamV = 1 };
 
-template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE, bool PART>
+template <int DQK, bool FP8, int STREAM, bool VARLEN, bool SLICE, bool PART, bool LIST>
 __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
-                            const AttnArgs& a, const Sched<VARLEN, PART>& sc, bool leader) {
+                            const AttnArgs& a, const Sched<VARLEN, PART, LIST>& sc, bool leader) {
   using C = Cfg<DQK, FP8>;
   constexpr bool kIsK = (STREAM == kStreamQK);
   constexpr int kStages = kIsK ? C::kNK : C::kNV;
   constexpr uint32_t kTileBytes = kIsK ? C::kQkTileBytes : C::kVTileBytes;
-  const int n_units = sc.n_units();
   const int group = a.Hq / a.Hkv;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = sm.abort_flag();
@@ -418,7 +434,7 @@ __device__ void loader_role(const Smem<DQK, FP8>& sm, const CUtensorMap* tm_q, c
   auto full = [&](int i) { return kIsK ? sm.k_full(i) : sm.v_full(i); };
   auto empty = [&](int i) { return kIsK ? sm.k_empty(i) : sm.v_empty(i); };
   auto tile = [&](int i) { return kIsK ? sm.k_tile(i) : sm.v_tile(i); };
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+  for (int i = 0, u = sc.first(); u >= 0 && ok; u = sc.next(++i, u)) {
     const Unit w = sc.decode(u);
     const int hkv = w.hq / group;
     if constexpr (kIsK) {
@@ -590,11 +606,10 @@ __device__ __forceinline__ void issue_pv(const OperandDescs& od, uint32_t tmem_p
 // The whole warp runs the schedule (waits, stage and phase bookkeeping,
 // descriptors: all warp-uniform); one elected lane issues tcgen05.mma and
 // tcgen05.commit, so a commit tracks exactly the MMAs of that lane.
-template <int DQK, bool FP8, bool VARLEN, bool PART>
-__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool PART, bool LIST>
+__device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART, LIST>& sc,
                          bool leader) {
   using C = Cfg<DQK, FP8>;
-  const int n_units = sc.n_units();
   volatile int* abort_flag = sm.abort_flag();
   const uint32_t tS0 = tmem, tS1 = tmem + 128;
   const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
@@ -617,7 +632,7 @@ __device__ void mma_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs
   if (!(ok = warp_wait((bar), (par), abort_flag, a.status, kStatusMmaTimeout, a.timeout_ns))) break; \
   tc_fence_after();
 
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+  for (int i = 0, u = sc.first(); u >= 0 && ok; u = sc.next(++i, u)) {
     const Unit w = sc.decode(u);
     do {
       ZYFA_WAIT(sm.q_full(), qn & 1u);
@@ -1042,10 +1057,9 @@ __device__ __forceinline__ void slice_probs(uint32_t tS, uint32_t tO, int cpy, b
   if (moved) rescale_o_row(tO, rho);
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART>
-__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART>& sc,
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART, bool LIST>
+__device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const AttnArgs& a, const Sched<VARLEN, PART, LIST>& sc,
                              int warp, int lane) {
-  const int n_units = sc.n_units();
   const int nblk = a.scale_blocks;
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = sm.abort_flag();
@@ -1062,7 +1076,7 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
   (void)tr;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o);
 
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (int i = 0, u = sc.first(); u >= 0; u = sc.next(++i, u)) {
     Unit w = sc.decode(u);
     if (wg == 1 && !w.has_b) continue;
     if constexpr (VARLEN) {
@@ -1336,19 +1350,23 @@ __device__ void softmax_role(const Smem<DQK, FP8>& sm, uint32_t tmem, const Attn
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART>
+// LIST: equal lengths with the host's per-CTA unit lists (a parameter of
+// about 17 KB, so calls of one wave keep the round-robin instantiation).
+struct NoList {};
+template <int DQK, bool FP8, bool VARLEN, bool LEAN, bool SLICE, bool PART, bool LIST>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a,
                     const __grid_constant__ typename Sched<VARLEN>::Table tab,
-                    const typename Sched<VARLEN>::Table* tab_global) {
+                    const typename Sched<VARLEN>::Table* tab_global,
+                    const __grid_constant__ typename std::conditional<LIST, UnitList, NoList>::type lst) {
   using C = Cfg<DQK, FP8>;
   extern __shared__ uint8_t smem_raw[];
   Smem<DQK, FP8> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Sched<VARLEN, PART> sc;
+  Sched<VARLEN, PART, LIST> sc;
   // The unit table comes by value (built on the host) or, when the sequence
   // offsets live on the device, from global memory (built by a kernel).
   sc.tab = tab_global ? tab_global : &tab;
@@ -1362,6 +1380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.groups_in_flight = max(1, a.groups_in_flight);
   sc.one_token = a.one_token != 0;
   sc.split_tiles = a.split_tiles;
+  if constexpr (LIST) sc.list = &lst;
+  else sc.list = nullptr;
+  sc.nu = sc.n_units();
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
@@ -1395,16 +1416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<RegSplit<FP8>::kControl>();
     const bool leader = elect_one_sync();
     if (warp == kLoadWarp) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE, PART>(sm, &tm_q, &tm_k, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamQK, VARLEN, SLICE, PART, LIST>(sm, &tm_q, &tm_k, a, sc, leader);
     } else if (warp == kLoadWarpV) {
-      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE, PART>(sm, &tm_q, &tm_v, a, sc, leader);
+      if (!a.debug_stall) loader_role<DQK, FP8, kStreamV, VARLEN, SLICE, PART, LIST>(sm, &tm_q, &tm_v, a, sc, leader);
     } else if (warp == kMmaWarp) {
       mma_role(sm, tmem, a, sc, leader);
     }
     __syncwarp();
   } else {
     regs_increase<RegSplit<FP8>::kSoftmax>();
-    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE, PART>(sm, tmem, a, sc, warp, lane);
+    softmax_role<DQK, FP8, VARLEN, LEAN, SLICE, PART, LIST>(sm, tmem, a, sc, warp, lane);
     __syncwarp();
   }
   tc_fence_before();
@@ -1415,12 +1436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false, bool PART = SLICE>
+template <int DQK, bool FP8, bool VARLEN, bool LEAN = false, bool SLICE = false, bool PART = SLICE, bool LIST = false>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                    const typename Sched<VARLEN>::Table& tab, long long n_units, cudaStream_t stream,
-                   const typename Sched<VARLEN>::Table* tab_global = nullptr) {
+                   const typename Sched<VARLEN>::Table* tab_global = nullptr,
+                   const typename std::conditional<LIST, UnitList, NoList>::type* lst = nullptr) {
   using C = Cfg<DQK, FP8>;
-  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE, PART>;
+  auto kern = attn_fwd_kernel<DQK, FP8, VARLEN, LEAN, SLICE, PART, LIST>;
   // The shared-memory opt-in is per function and device: set it once.
   static bool opted_in[64] = {};
   int dev = 0;
@@ -1433,7 +1455,8 @@ cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUten
   }
   if (n_units == 0) return cudaSuccess;
   const int grid = static_cast<int>(n_units < a.num_sms ? n_units : a.num_sms);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab, tab_global);
+  const typename std::conditional<LIST, UnitList, NoList>::type none{};
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, tab, tab_global, lst ? *lst : none);
   return cudaGetLastError();
 }
 
@@ -1444,19 +1467,31 @@ long long fixed_units(const AttnArgs& a) {
 }  // namespace
 
 cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const AttnArgs& a, cudaStream_t stream) {
+                             const AttnArgs& a, cudaStream_t stream, const UnitList* list) {
   const NoTable none{};
-  if (a.Dqk == 128) return launch<128, false, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
-  if (a.Dqk == 192) return launch<192, false, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
+  const long long n = fixed_units(a);
+  if (list && a.Dqk == 128)
+    return launch<128, false, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n, stream, nullptr, list);
+  if (list && a.Dqk == 192)
+    return launch<192, false, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n, stream, nullptr, list);
+  if (a.Dqk == 128) return launch<128, false, false>(tm_q, tm_k, tm_v, a, none, n, stream);
+  if (a.Dqk == 192) return launch<192, false, false>(tm_q, tm_k, tm_v, a, none, n, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                            const AttnArgs& a, cudaStream_t stream) {
+                            const AttnArgs& a, cudaStream_t stream, const UnitList* list) {
   const NoTable none{};
-  if (a.Dqk == 128 && a.lean_p) return launch<128, true, false, true>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
-  if (a.Dqk == 128) return launch<128, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
-  if (a.Dqk == 192) return launch<192, true, false>(tm_q, tm_k, tm_v, a, none, fixed_units(a), stream);
+  const long long n = fixed_units(a);
+  if (list && a.Dqk == 128 && a.lean_p)
+    return launch<128, true, false, true, false, false, true>(tm_q, tm_k, tm_v, a, none, n, stream, nullptr, list);
+  if (list && a.Dqk == 128)
+    return launch<128, true, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n, stream, nullptr, list);
+  if (list && a.Dqk == 192)
+    return launch<192, true, false, false, false, false, true>(tm_q, tm_k, tm_v, a, none, n, stream, nullptr, list);
+  if (a.Dqk == 128 && a.lean_p) return launch<128, true, false, true>(tm_q, tm_k, tm_v, a, none, n, stream);
+  if (a.Dqk == 128) return launch<128, true, false>(tm_q, tm_k, tm_v, a, none, n, stream);
+  if (a.Dqk == 192) return launch<192, true, false>(tm_q, tm_k, tm_v, a, none, n, stream);
   return cudaErrorInvalidValue;
 }
 

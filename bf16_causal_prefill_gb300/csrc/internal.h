@@ -86,6 +86,18 @@ struct SeqTable {
   int level_start[kMaxVarlenLevels + 1];   // first unit of each level
 };
 
+// Equal-length calls of more than one wave: the host assigns the units
+// (in the kernel's order, longest query-tile pairs first within each
+// super-group of KV groups) to CTAs one by one, each to the CTA with the
+// least work so far (list scheduling, as a dynamic queue would), and passes
+// each CTA's units here: CTA c runs unit[start[c]] .. unit[start[c+1]-1].
+constexpr int kMaxListCtas = 256;
+constexpr int kMaxListUnits = 8192;
+struct UnitList {
+  uint16_t start[kMaxListCtas + 1];
+  uint16_t unit[kMaxListUnits];
+};
+
 struct AttnArgs {
   int B, S, Hq, Hkv, Dqk, Dv;         // varlen: B = 1 and S = total tokens (the packed tensor)
   float scale_log2;        // softmax_scale * log2(e)
@@ -153,10 +165,12 @@ constexpr unsigned int kStatusBadPage = 0x20u;
 
 // tm_q/tm_k/tm_v: 4-D tiled maps (D, H, S, B), 128-byte swizzle, box of
 // 128 bytes x 1 head x 128 tokens x 1 batch.
+// list: the per-CTA unit lists (grid = a.num_sms CTAs), or null for the
+// round-robin order (CTA c runs units c, c + grid, ...).
 cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const AttnArgs& a, cudaStream_t stream);
+                             const AttnArgs& a, cudaStream_t stream, const UnitList* list = nullptr);
 cudaError_t launch_attn_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                            const AttnArgs& a, cudaStream_t stream);
+                            const AttnArgs& a, cudaStream_t stream, const UnitList* list = nullptr);
 // Packed variable-length batch: maps over (D, H, T, 1); `tab` as above.
 // Paged K/V (a.block_table set): tm_k/tm_v over (D, H, 128, num_pages) and
 // tab.ctx gives each sequence's cached tokens.

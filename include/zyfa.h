@@ -469,7 +469,8 @@ int zyfa_attn_fwd_fp8_paged(const void* q8, const float* q_scale, const void* k_
  *              caller (calls that can run concurrently need their own). With
  *              it, when the N*Hkv tasks would leave SMs idle, each task's key
  *              range is split (at least 8 key blocks per split, about four
- *              tasks per SM), and with Hq/Hkv <= 32 the group's rows are
+ *              tasks per SM), and with Hq/Hkv <= 32 and at least 16 tasks
+ *              the group's rows are
  *              replicated four times in the tile so that each softmax warp
  *              takes a quarter of every key block's columns; every split and
  *              copy writes its unnormalised rows with their offset and sum,

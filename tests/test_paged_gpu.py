@@ -256,14 +256,15 @@ def test_decode_call_matches_oracle_and_the_paged_prefill(Hq, Hkv, D, fp8):
     assert torch.equal(o, ref_gpu)
 
 
-@pytest.mark.parametrize("Hq,Hkv,D", [(16, 8, 128), (64, 1, 128), (64, 1, 192)])
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 8, 128), (8, 4, 128), (64, 1, 128), (64, 1, 192)])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_decode_small_batch_long_context_splits(Hq, Hkv, D, fp8):
     """Two sequences of 9000 and 20000 positions: a handful of tasks for the
     whole GPU, so the key ranges are split into many pieces; against the
     oracle, and within rounding of the unsplit call. 16/8 heads replicate the
-    group's rows in the tile; 64 query heads per KV head (above 32) take the
-    split path with one copy of the rows. Queries are scaled by 3 so the rows
+    group's rows in the tile; 8/4 heads (8 tasks, too few for replicated
+    rows) and 64 query heads per KV head (above 32) take the split path with
+    one copy of the rows. Queries are scaled by 3 so the rows
     attend to a few hundred keys rather than near-uniformly to all 20000 (a
     flat average of random values shrinks the output to the size of the FP8
     probability-rounding noise, split or not)."""
