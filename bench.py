@@ -510,7 +510,8 @@ def main():
     # Small problems split each query-tile pair's keys across CTAs (the
     # library decides; this workspace lets it): allocated once, outside the
     # timed steps. Large problems need none and run the unsplit kernels.
-    ws_bytes = 0 if args.no_split else zyfa.lib().zyfa_attn_workspace_bytes(w.B, w.S, w.Hq)
+    split_c = 0 if args.no_split else zyfa.lib().zyfa_attn_split_tiles(w.B, w.S, w.Hq)
+    ws_bytes = zyfa.lib().zyfa_attn_workspace_bytes(w.B, w.S, w.Hq) if split_c > 0 else 0
     split_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else False
 
     def fp8_step(ev_attn=None):
@@ -661,7 +662,7 @@ def main():
                    "path": ("fp8: quantise Q,K,V (1 launch) + fp8 causal attention with key ranges split "
                             "across CTAs (2 launches: chunks, combine)" if ws_bytes else
                             "fp8: quantise Q,K,V (1 launch) + fp8 causal attention (1 launch)"),
-                   "split_key_ranges": bool(ws_bytes),
+                   "split_key_ranges": bool(ws_bytes), "split_chunk_blocks": max(split_c, 0),
                    "hadamard": had, "parallelism": f"replicas x{world}",
                    "l2": "256 MiB flush between timed steps; inputs larger than L2"},
         "pct_of_peak": {"fp8_attention_kernel": a8 / fp8_peak, "fp8_step": v8 / world / fp8_peak,

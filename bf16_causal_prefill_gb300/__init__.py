@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
                                          c_float, vp, vp, vp, vp, c_int, c_int, c_int, vp]
     L.zyfa_attn_workspace_bytes.restype = ctypes.c_size_t
     L.zyfa_attn_workspace_bytes.argtypes = [c_int, c_int, c_int]
+    L.zyfa_attn_split_tiles.restype = c_int
+    L.zyfa_attn_split_tiles.argtypes = [c_int, c_int, c_int]
     L.zyfa_attn_fwd_bf16_ws.restype = c_int
     L.zyfa_attn_fwd_bf16_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                         vp, vp, vp, vp, vp, ctypes.c_size_t, vp]

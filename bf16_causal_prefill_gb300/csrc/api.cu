@@ -604,6 +604,14 @@ static int attn_common(bool fp8, int lean, const void* q, const float* qsc, cons
 
 size_t zyfa_attn_workspace_bytes(int B, int S, int Hq) { return prefill_ws_bytes(B, S, Hq); }
 
+int zyfa_attn_split_tiles(int B, int S, int Hq) {
+  if (B < 1 || S < 1 || Hq < 1) return -fail(ZYFA_ERR_INVALID_ARG, "B, S and Hq must be >= 1");
+  DeviceInfo* d;
+  if (int r = device_info(&d)) return -r;
+  long long units;
+  return prefill_split_tiles(B, S, Hq, d->sm_count, &units);
+}
+
 int zyfa_attn_fwd_bf16_ws(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
                           int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
                           const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],

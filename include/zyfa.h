@@ -219,6 +219,10 @@ int zyfa_attn_fwd_fp8(const void* q8, const float* q_scale, const void* k8, cons
  * Other arguments and errors as the calls above.
  */
 size_t zyfa_attn_workspace_bytes(int B, int S, int Hq);
+/* The chunk length C (key blocks) a full-sequence workspace call of these
+ * sizes would use on the current device, 0 when it runs unsplit; negative:
+ * minus a status code (B, S or Hq below 1: -ZYFA_ERR_INVALID_ARG). */
+int zyfa_attn_split_tiles(int B, int S, int Hq);
 int zyfa_attn_fwd_bf16_ws(const void* q, const void* k, const void* v, void* o, int B, int S, int Hq, int Hkv,
                           int Dqk, int Dv, float softmax_scale, const int64_t q_strides[3],
                           const int64_t k_strides[3], const int64_t v_strides[3], const int64_t o_strides[3],

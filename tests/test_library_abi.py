@@ -350,3 +350,8 @@ def test_attn_ws_calls_refuse_bad_arguments_before_launch(L):
     rc = L.zyfa_attn_fwd_bf16_ws(None, 16, 16, 16, 1, 128, 2, 2, 128, 128, ctypes.c_float(0.1), s3, s3, s3, s3,
                                  None, 0, None)
     assert rc == 1   # ZYFA_ERR_INVALID_ARG: null q
+
+
+def test_attn_split_tiles_refuses_bad_sizes(L):
+    assert L.zyfa_attn_split_tiles(0, 1024, 2) == -1
+    assert L.zyfa_attn_split_tiles(1, 0, 2) == -1

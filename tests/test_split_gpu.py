@@ -48,6 +48,7 @@ def _inputs(B, Hq, Hkv, S, D, seed):
 @pytest.mark.parametrize("B,Hq,Hkv,S,D", SHAPES)
 def test_split_bf16_matches_oracle(B, Hq, Hkv, S, D):
     assert zyfa.lib().zyfa_attn_workspace_bytes(B, S, Hq) > 0
+    assert zyfa.lib().zyfa_attn_split_tiles(B, S, Hq) > 0
     w, (q, k, v) = _inputs(B, Hq, Hkv, S, D, seed=S + 7)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = zyfa.attn_fwd_bf16(qd, kd, vd, w.softmax_scale, split=True)
@@ -85,6 +86,7 @@ def test_small_workload_does_not_split():
     q, k, v = workloads.make_qkv(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     assert zyfa.lib().zyfa_attn_workspace_bytes(w.B, w.S, w.Hq) > 0
+    assert zyfa.lib().zyfa_attn_split_tiles(w.B, w.S, w.Hq) == 0
     o1, _ = zyfa.prefill_fp8(qd, kd, vd, split=True)
     o2, _ = zyfa.prefill_fp8(qd, kd, vd)
     b1 = zyfa.attn_fwd_bf16(qd, kd, vd, split=True)
