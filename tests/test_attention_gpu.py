@@ -159,3 +159,27 @@ def test_rotation_keeps_attention():
     ref = oattn.causal_attention(f32(q), f32(k), f32(v), w.softmax_scale)
     assert oattn.rel_l2(f32(o_plain), ref) < 5e-2
     assert oattn.rel_l2(f32(o_rot), ref) < 5e-2
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_more_than_one_wave_with_odd_tile_count(fp8):
+    """16 query heads over 21 query tiles: 176 query-tile pairs, more than
+    one wave, so the units run from the host's per-CTA lists, and the last
+    pair of every head has no second tile. Full output against the oracle."""
+    B, Hq, Hkv, S, D = 1, 16, 4, 2688, 128
+    w, (q, k, v), (qd, kd, vd) = _inputs(B, Hq, Hkv, S, D, seed=77 + fp8)
+    if fp8:
+        cq, sq = oracle_quant(q, False)
+        ck, sk = oracle_quant(k, False)
+        cv, sv = oracle_quant(v, False)
+        dev = lambda a: torch.from_numpy(a).cuda()
+        o = zyfa.attn_fwd_fp8(dev(cq), dev(sq), dev(ck), dev(sk), dev(cv), dev(sv), w.softmax_scale)
+        ref = oattn.causal_attention(oracle_dequant(cq, sq), oracle_dequant(ck, sk), oracle_dequant(cv, sv),
+                                     w.softmax_scale)
+        zyfa.device_status()
+        assert_fp8_gate(f32(o), ref, "fp8 multi-wave odd tiles")
+    else:
+        o = zyfa.attn_fwd_bf16(qd, kd, vd, w.softmax_scale)
+        zyfa.device_status()
+        ref = oattn.causal_attention(f32(q), f32(k), f32(v), w.softmax_scale)
+        assert_bf16_gate(f32(o), ref, "bf16 multi-wave odd tiles")
