@@ -433,6 +433,10 @@ static long long schedule_cost(int B, int Hq, int nq, int sms, int C, long long*
   return cost;
 }
 
+// Problems of this many query-tile pairs or more never split, whatever the
+// SM count: the workspace size does not depend on the GPU.
+constexpr int kMaxSmsForPrefillSplit = 256;
+
 static int min_split_tiles(int nq) {
   const int c = (nq + kMaxKeyChunks - 1) / kMaxKeyChunks;
   return std::max(2, (c + 1) & ~1);
@@ -442,7 +446,7 @@ static int min_split_tiles(int nq) {
 static int prefill_split_tiles(int B, int S, int Hq, int sms, long long* units) {
   if (B < 1 || S < 1 || Hq < 1 || sms < 1) return 0;
   const int nq = (S + 127) / 128, pairs = (nq + 1) / 2;
-  if (static_cast<long long>(B) * Hq * pairs >= sms) return 0;
+  if (static_cast<long long>(B) * Hq * pairs >= std::min(sms, kMaxSmsForPrefillSplit)) return 0;
   long long n0;
   const long long plain = schedule_cost(B, Hq, nq, sms, 0, &n0);
   long long best = plain;
@@ -466,7 +470,6 @@ static int prefill_split_tiles(int B, int S, int Hq, int sms, long long* units) 
 // Hq, for problems of fewer than kMaxSmsForPrefillSplit pairs and more than
 // two query tiles (whether the call splits depends on the GPU's SM count);
 // 0 otherwise.
-constexpr int kMaxSmsForPrefillSplit = 256;
 static size_t prefill_partial_rows(int B, int S, int Hq) {
   if (B < 1 || S < 1 || Hq < 1) return 0;
   const int nq = (S + 127) / 128, pairs = (nq + 1) / 2;
