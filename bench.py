@@ -298,6 +298,40 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------------- main --
+def measure_fp8_gemm(dev, n: int = 8192, reps: int = 10):
+    """Burst rate of the library's dense e4m3 GEMM on this GPU: cuBLASLt
+    through torch._scaled_mm, n^3, tensor-wise scales, bf16 out, best of
+    `reps` after 3 warm-ups (the method of the measured bf16 figure). The
+    attention kernel is also compared with it; the roofline's peak stays the
+    measured bf16 burst x the nominal fp8/bf16 ratio. None if the library
+    call is not available."""
+    import torch
+    try:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        bt = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev, dtype=torch.float32)
+
+        def gemm():
+            return torch._scaled_mm(a, bt.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            gemm()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gemm()
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
+
 def main_reference(args):
     _pin_cpu_threads()
     world, rank, _ = dist_setup()
@@ -651,6 +685,7 @@ def main():
 
     if rank != 0:
         return
+    fp8_gemm = measure_fp8_gemm(dev)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(name, 12.0, had)
@@ -671,8 +706,13 @@ def main():
         "roofline": {"bound": "tensor", "achieved": a8, "peak": fp8_peak, "unit": UNIT, "frac": a8 / fp8_peak,
                      "traffic": tr8, "kernel": "attn_fwd_fp8",
                      "peak_note": (f"the fp8 peak is nominal: {src} bf16 burst {peaks['bf16_tflops']:g} TFLOP/s x "
-                                   f"{FP8_PER_BF16:g}, the nominal fp8/bf16 tensor-core ratio (no fp8 figure is "
-                                   f"measured); sustained-peak frac {a8 / fp8_peak_sus:.3f}"),
+                                   f"{FP8_PER_BF16:g}, the nominal fp8/bf16 tensor-core ratio; sustained-peak frac "
+                                   f"{a8 / fp8_peak_sus:.3f}; measured_fp8_gemm: the library's e4m3 GEMM "
+                                   f"timed in this run"),
+                     "measured_fp8_gemm": None if fp8_gemm is None else {
+                         "tflops": fp8_gemm, "frac": a8 / fp8_gemm,
+                         "how": "cuBLASLt e4m3 8192^3 GEMM (torch._scaled_mm, bf16 out), best of 10 after the "
+                                "timed steps"},
                      "ms_per_launch": t8k, "secondary": secondary},
         "bf16": {"value": v16, "unit": UNIT, "ms_per_step": t16, "dtype": "bf16", "gpu_launches": (2 if ws_bytes else 1) * K,
                  "roofline": {"bound": "tensor", "achieved": a16, "peak": peaks["bf16_tflops"], "unit": UNIT,
