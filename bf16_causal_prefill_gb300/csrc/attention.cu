@@ -382,7 +382,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // Warp-wide bounded wait on two barriers at once (one poll loop, one vote):
 // each wait costs the MMA warp a fixed overhead during which the tensor pipe
-// drains, so the two TMA barriers of an iteration share one.
+// drains, so the two TMA barriers of an iteration share one. The abort flag
+// and the clock are read every 64 polls, as in mbar_wait.
 __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64_t* bar2, uint32_t par2,
                                            volatile int* abort_flag, unsigned int* status, unsigned int code,
                                            uint64_t timeout_ns) {
@@ -393,11 +394,13 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar1, uint32_t par1, uint64
       if (!ok1) ok1 = mbar_try_wait(bar1, par1);
       if (!ok2) ok2 = mbar_try_wait(bar2, par2);
       if (ok1 && ok2) break;
-      if (*abort_flag) break;
-      if ((it & 63u) == 0 && global_timer_ns() - t0 > timeout_ns) {
-        *abort_flag = 1;
-        if (status) atomicOr(status, code);
-        break;
+      if ((it & 63u) == 0) {
+        if (*abort_flag) break;
+        if (global_timer_ns() - t0 > timeout_ns) {
+          *abort_flag = 1;
+          if (status) atomicOr(status, code);
+          break;
+        }
       }
     }
   }

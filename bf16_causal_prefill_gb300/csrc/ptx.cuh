@@ -72,18 +72,23 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait. Returns false if the CTA-wide abort flag is raised or the wait
 // exceeds `timeout_ns`; in the latter case this thread raises the abort flag
-// and ORs `code` into the device status word. Never spins forever.
+// and ORs `code` into the device status word. Never spins forever. The flag
+// and the clock are read every 64 polls, so a poll that misses is followed at
+// once by the next (reading the flag after each one delayed the hand-offs of
+// the attention kernel measurably).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status, unsigned int code, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > timeout_ns) {
-      *abort_flag = 1;
-      if (status) atomicOr(status, code);
-      return false;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, code);
+        return false;
+      }
     }
   }
 }
