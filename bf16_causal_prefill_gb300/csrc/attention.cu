@@ -352,25 +352,32 @@ struct Sched {
 template <int DQK, bool FP8>
 struct Smem {
   using C = Cfg<DQK, FP8>;
-  uint8_t* base;
-  uint64_t* bars;
-  __device__ __forceinline__ uint64_t* q_full() const { return bars; }
-  __device__ __forceinline__ uint64_t* q_empty() const { return bars + 1; }
-  __device__ __forceinline__ uint64_t* k_full(int s) const { return bars + 2 + s; }
-  __device__ __forceinline__ uint64_t* k_empty(int s) const { return bars + 2 + C::kNK + s; }
-  __device__ __forceinline__ uint64_t* v_full(int s) const { return bars + 2 + 2 * C::kNK + s; }
-  __device__ __forceinline__ uint64_t* v_empty(int s) const { return bars + 2 + 2 * C::kNK + C::kNV + s; }
-  __device__ __forceinline__ uint64_t* s_full(int t) const { return bars + 2 + 2 * C::kNK + 2 * C::kNV + t; }
-  __device__ __forceinline__ uint64_t* p_full(int t) const { return s_full(2) + t; }
-  __device__ __forceinline__ uint64_t* o_full(int t) const { return s_full(4) + t; }
-  __device__ __forceinline__ uint64_t* drain() const { return s_full(6); }
-  __device__ __forceinline__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars + C::kNumBars); }
-  __device__ __forceinline__ volatile int* abort_flag() const {
-    return reinterpret_cast<volatile int*>(bars + C::kNumBars) + 1;
+  // Shared-window address of the 1024-byte aligned base: one 32-bit value;
+  // the generic pointers below are formed from it where they are used.
+  uint32_t sb;
+  __device__ __forceinline__ uint8_t* at(uint32_t off) const {
+    return static_cast<uint8_t*>(__cvta_shared_to_generic(static_cast<size_t>(sb + off)));
   }
-  __device__ __forceinline__ uint8_t* q_tile(int t) const { return base + C::kOffQ + t * C::kQkTileBytes; }
-  __device__ __forceinline__ uint8_t* k_tile(int s) const { return base + C::kOffK + s * C::kQkTileBytes; }
-  __device__ __forceinline__ uint8_t* v_tile(int s) const { return base + C::kOffV + s * C::kVTileBytes; }
+  __device__ __forceinline__ uint64_t* bar(int i) const {
+    return reinterpret_cast<uint64_t*>(at(C::kOffBar + 8u * static_cast<uint32_t>(i)));
+  }
+  __device__ __forceinline__ uint64_t* q_full() const { return bar(0); }
+  __device__ __forceinline__ uint64_t* q_empty() const { return bar(1); }
+  __device__ __forceinline__ uint64_t* k_full(int s) const { return bar(2 + s); }
+  __device__ __forceinline__ uint64_t* k_empty(int s) const { return bar(2 + C::kNK + s); }
+  __device__ __forceinline__ uint64_t* v_full(int s) const { return bar(2 + 2 * C::kNK + s); }
+  __device__ __forceinline__ uint64_t* v_empty(int s) const { return bar(2 + 2 * C::kNK + C::kNV + s); }
+  __device__ __forceinline__ uint64_t* s_full(int t) const { return bar(2 + 2 * C::kNK + 2 * C::kNV + t); }
+  __device__ __forceinline__ uint64_t* p_full(int t) const { return s_full(2 + t); }
+  __device__ __forceinline__ uint64_t* o_full(int t) const { return s_full(4 + t); }
+  __device__ __forceinline__ uint64_t* drain() const { return s_full(6); }
+  __device__ __forceinline__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bar(C::kNumBars)); }
+  __device__ __forceinline__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(bar(C::kNumBars)) + 1;
+  }
+  __device__ __forceinline__ uint8_t* q_tile(int t) const { return at(C::kOffQ + t * C::kQkTileBytes); }
+  __device__ __forceinline__ uint8_t* k_tile(int s) const { return at(C::kOffK + s * C::kQkTileBytes); }
+  __device__ __forceinline__ uint8_t* v_tile(int s) const { return at(C::kOffV + s * C::kVTileBytes); }
 };
 
 // Warp-wide bounded wait: every lane polls; the result is uniform.
@@ -1366,8 +1373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<DQK, FP8>;
   extern __shared__ uint8_t smem_raw[];
   Smem<DQK, FP8> sm;
-  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  sm.bars = reinterpret_cast<uint64_t*>(sm.base + C::kOffBar);
+  sm.sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Sched<VARLEN, PART, LIST> sc;
   // The unit table comes by value (built on the host) or, when the sequence
