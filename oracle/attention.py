@@ -9,11 +9,15 @@ heads as in the Mistral-7B / Qwen3-8B layers it times):
     O[b, i, h, :] = sum_{j <= i} softmax_j( scale * Q[b,i,h] . K[b,j,g(h)] ) V[b,j,g(h)]
     g(h) = h // (Hq / Hkv)
 
-The softmax subtracts the row maximum before exponentiating. Nothing here
-models FP8 probabilities, lean P or any kernel-internal rounding: for the FP8
-path the oracle is this same definition applied to the dequantised inputs
-(the ZYFA post, "Error of a Single Attention Call", compares kernels with fp64
-attention on the same quantised inputs).
+The softmax subtracts the row maximum before exponentiating. For the FP8
+path the parity gate is this same definition applied to the dequantised
+inputs (the ZYFA post, "Error of a Single Attention Call", compares kernels
+with fp64 attention on the same quantised inputs). Two further functions
+round the probabilities: causal_attention_rows_pquant the way the pages
+describe (per-64-key powers of two; the error-by-stage report), and
+causal_attention_rows_window under the per-row offset window, the reading of
+that scheme the GB300 FP8 path follows (a tighter check of its rounding).
+Nothing here models lean P.
 """
 from __future__ import annotations
 
@@ -155,6 +159,89 @@ def causal_attention_rows_pquant(q: np.ndarray, k: np.ndarray, v: np.ndarray, sc
             codes = _fp8.e4m3_rne(np.ldexp(pb, kb))
             w[c:c + block] = np.ldexp(_fp8.e4m3_decode(codes), -kb)
         res.append((w @ vv) / np.sum(w))
+    return np.stack(res)
+
+
+# The probability rounding of the GB300 FP8 path, a reading of the ZYFA post
+# ("Per-Block Scaling and Normalization by the Rounded Row Sum") for a tensor
+# core that applies no per-row scale inside the PV product: each row keeps one
+# power-of-two offset o for all its key tiles, moved (with the partial output
+# and sum rescaled by the exact power of two) only when a tile's largest
+# scaled probability leaves [2^WIN_LO, 2^WIN_HI]; o never drops more than
+# WIN_FLOOR binades below the row's largest log2 value seen so far.
+WIN_LO, WIN_HI, WIN_FLOOR = -4.0, 8.0, 64.0
+
+
+def window_step(o: Optional[float], top: Optional[float], bm: float):
+    """One key tile of the offset rule. bm: log2 of the tile's largest
+    scaled probability before the offset (its largest base-2 score plus
+    log2 of the tile's V scale); o, top: the row's offset and largest bm so
+    far (None before the first tile). Returns the new (o, top): the first
+    tile sets o = bm; a later tile moves o to max(bm, max(top, bm) - WIN_FLOOR)
+    when bm - o > WIN_HI, or when bm - o < WIN_LO while bm lies within
+    WIN_FLOOR binades of top; otherwise o stays."""
+    if o is None:
+        return bm, bm
+    rel = bm - o
+    if rel > WIN_HI or (rel < WIN_LO and bm > top - WIN_FLOOR):
+        o = max(bm, max(top, bm) - WIN_FLOOR)
+    return o, max(top, bm)
+
+
+def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray, ks: np.ndarray,
+                                 v8: np.ndarray, vs: np.ndarray, scale: float, b: int, h: int,
+                                 rows: Iterable[int], block: int = 128, round_p: bool = True,
+                                 trace: Optional[list] = None) -> np.ndarray:
+    """Selected output rows of the FP8 path with the probabilities rounded
+    under the offset window above. Inputs are the e4m3 codes [B,S,H,D] and
+    the per-(batch, head, 128-token block) scales [B,H,nblk] of Q, K, V.
+
+    For row i, key tiles j = 0 .. i // block in order (tile j: keys j*block ..
+    min(j*block + block, i + 1) - 1): base-2 scores x = (q_code . k_code) *
+    sq * sk * scale / ln 2; bm = max x + log2 sv; the offset o follows
+    window_step; the tile's probabilities P' = e4m3_RNE(2^(x + log2 sv - o))
+    (unrounded when round_p is False); with earlier tiles scaled by
+    2^(o_old - o) at each move, O = sum P' v_code and l = sum P' / sv, and
+    the row's output is O / l. The weight on the dequantised value v_code * sv
+    is P' 2^o / sv, so the weights sum to one exactly: the output is
+    normalised by the sum of the rounded probabilities. With round_p False
+    this is exact softmax attention on the dequantised inputs. trace, if
+    given, receives (i, j, o) for every tile. Returns [len(rows), Dv] float64."""
+    from . import fp8 as _fp8
+
+    Hq = q8.shape[2]
+    Hkv = k8.shape[2]
+    g = kv_head(h, Hq, Hkv)
+    c2 = scale / math.log(2.0)
+    res = []
+    for i in rows:
+        qc = _fp8.e4m3_decode(q8[b, i, h, :])
+        sq = float(qs[b, h, i // block])
+        o = top = None
+        acc = np.zeros(v8.shape[3], dtype=np.float64)
+        l = 0.0
+        for j in range(i // block + 1):
+            k0, k1 = j * block, min(j * block + block, i + 1)
+            kc = _fp8.e4m3_decode(k8[b, k0:k1, g, :])
+            vc = _fp8.e4m3_decode(v8[b, k0:k1, g, :])
+            sk, sv = float(ks[b, g, j]), float(vs[b, g, j])
+            x = (kc @ qc) * (sq * sk * c2)
+            lsv = math.log2(sv)
+            bm = float(np.max(x)) + lsv
+            o_new, top = window_step(o, top, bm)
+            if o is not None and o_new != o:
+                f = 2.0 ** (o - o_new)
+                acc *= f
+                l *= f
+            o = o_new
+            p = np.exp2(x + lsv - o)
+            if round_p:
+                p = _fp8.e4m3_decode(_fp8.e4m3_rne(p))
+            acc += p @ vc
+            l += float(np.sum(p)) / sv
+            if trace is not None:
+                trace.append((i, j, o))
+        res.append(acc / l)
     return np.stack(res)
 
 
