@@ -188,10 +188,42 @@ def window_step(o: Optional[float], top: Optional[float], bm: float):
     return o, max(top, bm)
 
 
+def _window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j_lo, j_hi, block, round_p, trace):
+    """Row i over key tiles j_lo .. j_hi - 1 in order, starting a fresh
+    offset: returns (O, l, o) in units of the final offset o."""
+    from . import fp8 as _fp8
+
+    o = top = None
+    acc = np.zeros(v8.shape[3], dtype=np.float64)
+    l = 0.0
+    for j in range(j_lo, j_hi):
+        k0, k1 = j * block, min(j * block + block, i + 1)
+        kc = _fp8.e4m3_decode(k8[b, k0:k1, g, :])
+        vc = _fp8.e4m3_decode(v8[b, k0:k1, g, :])
+        sk, sv = float(ks[b, g, j]), float(vs[b, g, j])
+        x = (kc @ qc) * (sq * sk * c2)
+        lsv = math.log2(sv)
+        bm = float(np.max(x)) + lsv
+        o_new, top = window_step(o, top, bm)
+        if o is not None and o_new != o:
+            f = 2.0 ** (o - o_new)
+            acc *= f
+            l *= f
+        o = o_new
+        p = np.exp2(x + lsv - o)
+        if round_p:
+            p = _fp8.e4m3_decode(_fp8.e4m3_rne(p))
+        acc += p @ vc
+        l += float(np.sum(p)) / sv
+        if trace is not None:
+            trace.append((i, j, o))
+    return acc, l, o
+
+
 def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray, ks: np.ndarray,
                                  v8: np.ndarray, vs: np.ndarray, scale: float, b: int, h: int,
                                  rows: Iterable[int], block: int = 128, round_p: bool = True,
-                                 trace: Optional[list] = None) -> np.ndarray:
+                                 trace: Optional[list] = None, chunk_tiles: int = 0) -> np.ndarray:
     """Selected output rows of the FP8 path with the probabilities rounded
     under the offset window above. Inputs are the e4m3 codes [B,S,H,D] and
     the per-(batch, head, 128-token block) scales [B,H,nblk] of Q, K, V.
@@ -205,8 +237,13 @@ def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray,
     the row's output is O / l. The weight on the dequantised value v_code * sv
     is P' 2^o / sv, so the weights sum to one exactly: the output is
     normalised by the sum of the rounded probabilities. With round_p False
-    this is exact softmax attention on the dequantised inputs. trace, if
-    given, receives (i, j, o) for every tile. Returns [len(rows), Dv] float64."""
+    this is exact softmax attention on the dequantised inputs.
+
+    chunk_tiles = C > 0: the key range split into chunks of C tiles (tiles
+    cC .. min(cC + C, i // block + 1) - 1), each run as above from a fresh
+    offset, and the chunks' (O_c, l_c, o_c) merged exactly: with M = max o_c,
+    output = sum O_c 2^(o_c - M) / sum l_c 2^(o_c - M). trace, if given,
+    receives (i, j, o) for every tile. Returns [len(rows), Dv] float64."""
     from . import fp8 as _fp8
 
     Hq = q8.shape[2]
@@ -217,30 +254,13 @@ def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray,
     for i in rows:
         qc = _fp8.e4m3_decode(q8[b, i, h, :])
         sq = float(qs[b, h, i // block])
-        o = top = None
-        acc = np.zeros(v8.shape[3], dtype=np.float64)
-        l = 0.0
-        for j in range(i // block + 1):
-            k0, k1 = j * block, min(j * block + block, i + 1)
-            kc = _fp8.e4m3_decode(k8[b, k0:k1, g, :])
-            vc = _fp8.e4m3_decode(v8[b, k0:k1, g, :])
-            sk, sv = float(ks[b, g, j]), float(vs[b, g, j])
-            x = (kc @ qc) * (sq * sk * c2)
-            lsv = math.log2(sv)
-            bm = float(np.max(x)) + lsv
-            o_new, top = window_step(o, top, bm)
-            if o is not None and o_new != o:
-                f = 2.0 ** (o - o_new)
-                acc *= f
-                l *= f
-            o = o_new
-            p = np.exp2(x + lsv - o)
-            if round_p:
-                p = _fp8.e4m3_decode(_fp8.e4m3_rne(p))
-            acc += p @ vc
-            l += float(np.sum(p)) / sv
-            if trace is not None:
-                trace.append((i, j, o))
+        n = i // block + 1
+        C = chunk_tiles if chunk_tiles > 0 else n
+        parts = [_window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j0, min(j0 + C, n), block, round_p, trace)
+                 for j0 in range(0, n, C)]
+        M = max(o for _, _, o in parts)
+        acc = sum(a * 2.0 ** (o - M) for a, _, o in parts)
+        l = sum(x * 2.0 ** (o - M) for _, x, o in parts)
         res.append(acc / l)
     return np.stack(res)
 

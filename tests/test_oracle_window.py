@@ -112,3 +112,23 @@ def test_tile_maxima_stay_in_the_window():
             rel = bm - o
             assert rel <= oattn.WIN_HI + 1e-9
             assert rel >= oattn.WIN_LO - 1e-9 or bm <= t - oattn.WIN_FLOOR + 1e-9 or j == 0
+
+
+@pytest.mark.parametrize("w", CASES[::2], ids=lambda w: w.name)
+def test_chunked_window_merges_exactly(w):
+    """Key chunks run from fresh offsets and merged by their offsets: exact
+    attention with the rounding off (any chunk size), and the unchunked
+    emulation itself when one chunk holds every tile."""
+    (cq, sq), (ck, sk), (cv, sv) = _quantised(w)
+    dq, dk, dv = (ofp8.dequantize_fp8(c, s) for c, s in ((cq, sq), (ck, sk), (cv, sv)))
+    rows = sorted(r for r in set([0, 127, 128, 383, 384, w.S - 1] + list(range(7, w.S, 53))) if r < w.S)
+    for h in range(w.Hq):
+        ex = oattn.causal_attention_rows(dq, dk, dv, w.softmax_scale, 0, h, rows)
+        for C in (1, 2, 3):
+            un = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, h, rows,
+                                                    round_p=False, chunk_tiles=C)
+            assert oattn.rel_l2(un, ex) < 1e-12
+        whole = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, h, rows)
+        one = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, h, rows,
+                                                 chunk_tiles=64)
+        assert np.array_equal(whole, one)

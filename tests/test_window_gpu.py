@@ -18,7 +18,8 @@ import torch
 import bf16_causal_prefill_gb300 as zyfa
 import workloads
 from oracle import attention as oattn
-from parity import oracle_dequant, oracle_quant
+from oracle import fp8 as ofp8
+from parity import f32, oracle_dequant, oracle_quant
 
 pytestmark = pytest.mark.gpu
 
@@ -70,3 +71,69 @@ def test_fp8_rounding_matches_the_window_emulation(w):
     assert f_emu >= 0.97
     if not w.outliers:
         assert f_emu > f_exact + 0.3
+
+
+def _match(got: np.ndarray, emu: np.ndarray) -> float:
+    return float(np.mean(got == _bf16(emu)))
+
+
+def test_split_key_ranges_match_the_chunked_emulation():
+    """A call that splits each query-tile pair's keys into chunks of C tiles
+    (zyfa_attn_split_tiles): every chunk starts its own offset and the
+    partial rows are merged by their offsets, as the chunked emulation
+    does."""
+    w = workloads.custom(1, 1, 1, 4096, seed=35)
+    C = zyfa.lib().zyfa_attn_split_tiles(w.B, w.S, w.Hq)
+    assert C > 0
+    q, k, v = workloads.make_qkv(w)
+    (cq, sq), (ck, sk), (cv, sv) = (oracle_quant(x, False) for x in (q, k, v))
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o = zyfa.attn_fwd_fp8(dev(cq), dev(sq), dev(ck), dev(sk), dev(cv), dev(sv), w.softmax_scale, split=True)
+    zyfa.device_status()
+    got = o.float().cpu().numpy().astype(np.float64)
+    rows = sorted(set([0, 127, 128, 1023, 1024, w.S - 1] + list(range(9, w.S, 29))))
+    g = got[0, rows, 0, :]
+    chunked = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, 0, rows, chunk_tiles=C)
+    whole = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, 0, rows)
+    f_chunked, f_whole = _match(g, chunked), _match(g, whole)
+    print(f"\nsplit into chunks of {C} tiles: bitwise equal to the chunked emulation {f_chunked:.4f}, "
+          f"to the unchunked one {f_whole:.4f}")
+    assert oattn.rel_l2(g, chunked) < 3e-3
+    assert f_chunked >= 0.97
+
+
+def test_packed_batch_matches_the_window_emulation():
+    """Packed sequences (host offsets): each sequence's keys are tiled from
+    its own start and quantised on their own, so each sequence is the dense
+    emulation on its slice."""
+    lens, Hq, Hkv, D = [300, 1000, 129, 700], 4, 2, 128
+    gen = torch.Generator().manual_seed(36)
+    T = sum(lens)
+    q, k, v = (torch.randn(T, H, D, generator=gen).to(torch.bfloat16) for H in (Hq, Hkv, Hkv))
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    o, (q8, qs, k8, ks, v8, vs) = zyfa.prefill_fp8_varlen(q.cuda(), k.cuda(), v.cuda(), cu)
+    zyfa.device_status()
+    got = o.float().cpu().numpy().astype(np.float64)
+    codes = []
+    for x, gc in ((q, q8), (k, k8), (v, v8)):
+        rc, rs = ofp8.quantize_fp8_varlen(f32(x), cu)
+        np.testing.assert_array_equal(gc.cpu().numpy(), rc)
+        codes.append((rc, rs))
+    (cq, sq), (ck, sk), (cv, sv) = codes
+    scale = 1.0 / np.sqrt(D)
+    eq = n = 0
+    for i, L in enumerate(lens):
+        s0, nb = cu[i], (L + 127) // 128
+        sl = lambda c: c[s0:s0 + L][None]
+        rows = sorted(set([0, L - 1] + list(range(3, L, 41))))
+        for h in range(Hq):
+            emu = oattn.causal_attention_rows_window(sl(cq), sq[i:i + 1, :, :nb], sl(ck), sk[i:i + 1, :, :nb],
+                                                     sl(cv), sv[i:i + 1, :, :nb], scale, 0, h, rows)
+            gr = got[[s0 + r for r in rows], h, :]
+            assert oattn.rel_l2(gr, emu) < 3e-3
+            eq += int(np.sum(gr == _bf16(emu)))
+            n += gr.size
+    print(f"\npacked batch {lens}: bitwise equal to the emulation {eq / n:.4f}")
+    assert eq / n >= 0.97
