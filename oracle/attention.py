@@ -265,6 +265,69 @@ def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray,
     return np.stack(res)
 
 
+# The BF16 path's probabilities (a reading of the ZYFA post's normalisation
+# by the rounded row sum, carried over to BF16): a running maximum m kept
+# stale while no tile's maximum exceeds it by more than BF16_STALE binades,
+# probabilities 2^(x - m) rounded to bf16 before the PV product, and the row
+# sum taken over the rounded values.
+BF16_STALE = 8.0
+
+
+def bf16_rne(x: np.ndarray) -> np.ndarray:
+    """Finite non-negative values rounded to float32, then to bf16 (nearest,
+    ties to even), returned as float64."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def stale_max_step(m: Optional[float], xmax: float) -> float:
+    """One key tile of the BF16 running maximum: the first tile sets m to
+    its maximum; a later tile moves m to its own maximum only when that
+    exceeds m by more than BF16_STALE."""
+    if m is None or xmax > m + BF16_STALE:
+        return xmax
+    return m
+
+
+def causal_attention_rows_bf16(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, b: int, h: int,
+                               rows: Iterable[int], block: int = 128, round_p: bool = True) -> np.ndarray:
+    """Selected output rows of the BF16 path with its probability rounding:
+    for row i, key tiles j = 0 .. i // block in order, base-2 scores
+    x = (q . k) * scale / ln 2, m from stale_max_step (earlier tiles scaled by
+    2^(m_old - m) when it moves), P = bf16(2^(x - m)) (unrounded when
+    round_p is False), O = sum P v, l = sum P, output O / l: the weights sum
+    to one exactly. With round_p False this is exact softmax attention.
+    Returns [len(rows), Dv] float64."""
+    Hq = q.shape[2]
+    Hkv = k.shape[2]
+    g = kv_head(h, Hq, Hkv)
+    c2 = scale / math.log(2.0)
+    res = []
+    for i in rows:
+        qi = np.asarray(q[b, i, h, :], dtype=np.float64)
+        m = None
+        acc = np.zeros(v.shape[3], dtype=np.float64)
+        l = 0.0
+        for j in range(i // block + 1):
+            k0, k1 = j * block, min(j * block + block, i + 1)
+            x = (np.asarray(k[b, k0:k1, g, :], dtype=np.float64) @ qi) * c2
+            m_new = stale_max_step(m, float(np.max(x)))
+            if m is not None and m_new != m:
+                f = 2.0 ** (m - m_new)
+                acc *= f
+                l *= f
+            m = m_new
+            p = np.exp2(x - m)
+            if round_p:
+                p = bf16_rne(p)
+            acc += p @ np.asarray(v[b, k0:k1, g, :], dtype=np.float64)
+            l += float(np.sum(p))
+        res.append(acc / l)
+    return np.stack(res)
+
+
 def rel_l2(out: np.ndarray, ref: np.ndarray) -> float:
     """||out - ref||_2 / ||ref||_2 -- the relative RMS error of the ZYFA post
     ("Error of a Single Attention Call")."""
