@@ -12,12 +12,13 @@ heads as in the Mistral-7B / Qwen3-8B layers it times):
 The softmax subtracts the row maximum before exponentiating. For the FP8
 path the parity gate is this same definition applied to the dequantised
 inputs (the ZYFA post, "Error of a Single Attention Call", compares kernels
-with fp64 attention on the same quantised inputs). Two further functions
+with fp64 attention on the same quantised inputs). Three further functions
 round the probabilities: causal_attention_rows_pquant the way the pages
-describe (per-64-key powers of two; the error-by-stage report), and
+describe (per-64-key powers of two; the error-by-stage report),
 causal_attention_rows_window under the per-row offset window, the reading of
-that scheme the GB300 FP8 path follows (a tighter check of its rounding).
-Nothing here models lean P.
+that scheme the GB300 FP8 path follows, and causal_attention_rows_bf16, the
+BF16 path's stale running maximum with bf16 probabilities and their rounded
+sum (tighter checks of the two paths' rounding). Nothing here models lean P.
 """
 from __future__ import annotations
 
