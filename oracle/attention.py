@@ -189,7 +189,20 @@ def window_step(o: Optional[float], top: Optional[float], bm: float):
     return o, max(top, bm)
 
 
-def _window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j_lo, j_hi, block, round_p, trace):
+def lean_codes(y: np.ndarray) -> np.ndarray:
+    """Lean P ("Lean P: Linear Approximation of the FP8 Code" in the ZYFA
+    post): the e4m3 code of 2^t is taken as 8t + 56, which is exact at whole
+    t (the code grows by 8 per doubling and 56 encodes 1.0). Here
+    y = 1080 + 8t is rounded to the nearest integer, ties to even (float16
+    has unit spacing in [1024, 2048)), values below 1024 give code 0, and the
+    code is y - 1024. Returns the codes as uint8."""
+    y = np.asarray(y, dtype=np.float64)
+    n = np.rint(y)                              # nearest, ties to even
+    n = np.where(y < 1023.5, 1024.0, n)
+    return (n - 1024.0).astype(np.uint8)
+
+
+def _window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j_lo, j_hi, block, round_p, trace, lean=False):
     """Row i over key tiles j_lo .. j_hi - 1 in order, starting a fresh
     offset: returns (O, l, o) in units of the final offset o."""
     from . import fp8 as _fp8
@@ -211,9 +224,12 @@ def _window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j_lo, j_hi, block, round_
             acc *= f
             l *= f
         o = o_new
-        p = np.exp2(x + lsv - o)
-        if round_p:
-            p = _fp8.e4m3_decode(_fp8.e4m3_rne(p))
+        if lean:
+            p = _fp8.e4m3_decode(lean_codes(1080.0 + 8.0 * (x + lsv - o)))
+        else:
+            p = np.exp2(x + lsv - o)
+            if round_p:
+                p = _fp8.e4m3_decode(_fp8.e4m3_rne(p))
         acc += p @ vc
         l += float(np.sum(p)) / sv
         if trace is not None:
@@ -224,7 +240,8 @@ def _window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j_lo, j_hi, block, round_
 def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray, ks: np.ndarray,
                                  v8: np.ndarray, vs: np.ndarray, scale: float, b: int, h: int,
                                  rows: Iterable[int], block: int = 128, round_p: bool = True,
-                                 trace: Optional[list] = None, chunk_tiles: int = 0) -> np.ndarray:
+                                 trace: Optional[list] = None, chunk_tiles: int = 0,
+                                 lean: bool = False) -> np.ndarray:
     """Selected output rows of the FP8 path with the probabilities rounded
     under the offset window above. Inputs are the e4m3 codes [B,S,H,D] and
     the per-(batch, head, 128-token block) scales [B,H,nblk] of Q, K, V.
@@ -243,8 +260,11 @@ def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray,
     chunk_tiles = C > 0: the key range split into chunks of C tiles (tiles
     cC .. min(cC + C, i // block + 1) - 1), each run as above from a fresh
     offset, and the chunks' (O_c, l_c, o_c) merged exactly: with M = max o_c,
-    output = sum O_c 2^(o_c - M) / sum l_c 2^(o_c - M). trace, if given,
-    receives (i, j, o) for every tile. Returns [len(rows), Dv] float64."""
+    output = sum O_c 2^(o_c - M) / sum l_c 2^(o_c - M). lean: P' from
+    lean_codes(1080 + 8 (x + log2 sv - o)) instead of the rounded
+    exponential (same offsets, same normalisation by the sum of P'). trace,
+    if given, receives (i, j, o) for every tile. Returns [len(rows), Dv]
+    float64."""
     from . import fp8 as _fp8
 
     Hq = q8.shape[2]
@@ -257,7 +277,8 @@ def causal_attention_rows_window(q8: np.ndarray, qs: np.ndarray, k8: np.ndarray,
         sq = float(qs[b, h, i // block])
         n = i // block + 1
         C = chunk_tiles if chunk_tiles > 0 else n
-        parts = [_window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j0, min(j0 + C, n), block, round_p, trace)
+        parts = [_window_tiles(qc, sq, k8, ks, v8, vs, c2, b, g, i, j0, min(j0 + C, n), block, round_p, trace,
+                               lean)
                  for j0 in range(0, n, C)]
         M = max(o for _, _, o in parts)
         acc = sum(a * 2.0 ** (o - M) for a, _, o in parts)

@@ -132,3 +132,43 @@ def test_chunked_window_merges_exactly(w):
         one = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, h, rows,
                                                  chunk_tiles=64)
         assert np.array_equal(whole, one)
+
+
+def _page_codes():
+    codes = {}
+    import os
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "e4m3_page_values.txt")):
+        if line.strip() and not line.startswith("#"):
+            val, code = line.split()[:2]
+            codes[float(val)] = int(code, 16)
+    return codes
+
+
+def test_lean_codes_at_whole_exponents_are_the_pages_codes():
+    page = _page_codes()
+    for t, v in ((0, 1.0), (1, 2.0), (2, 4.0)):
+        assert int(oattn.lean_codes(np.array([1080.0 + 8 * t]))[0]) == page[v]
+    t = np.arange(-6, 9, dtype=np.float64)
+    assert np.array_equal(ofp8.e4m3_decode(oattn.lean_codes(1080.0 + 8 * t)), 2.0 ** t)
+
+
+def test_lean_code_is_the_exact_code_or_the_next():
+    """8 t + 56 rounds to the exact nearest code of 2^t or one above it: the
+    linear code overshoots the mantissa 8 (2^f - 1) by at most
+    8 max(f - 2^f + 1) < 0.7 (format definition, normal range)."""
+    t = np.linspace(-6.0, 8.0, 200001)
+    lean = oattn.lean_codes(1080.0 + 8.0 * t).astype(int)
+    exact = ofp8.e4m3_rne(2.0 ** t).astype(int)
+    d = lean - exact
+    assert d.min() == 0 and d.max() == 1
+    assert 0.2 < np.mean(d) < 0.6
+
+
+def test_lean_window_keeps_the_exact_average():
+    w = workloads.custom(1, 2, 1, 520, seed=25)
+    (cq, sq), (ck, sk), _ = _quantised(w)
+    c = 448.0 * 2.0 ** -3
+    cv, sv = ofp8.quantize_fp8(np.full((1, w.S, 1, 128), c, dtype=np.float32))
+    rows = [0, 5, 127, 128, 300, 519]
+    out = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, 1, rows, lean=True)
+    assert np.all(out == c)
