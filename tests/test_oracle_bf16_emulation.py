@@ -56,3 +56,46 @@ def test_rounded_sum_gives_exact_average():
     v = np.full((1, w.S, 1, 128), c)
     out = oattn.causal_attention_rows_bf16(q, k, v, w.softmax_scale, 0, 1, [0, 5, 127, 128, w.S - 1])
     assert np.all(out == c)
+
+
+# ---------------------------------------------------------------- mutations --
+
+def _bf16_mutant(q, k, v, scale, b, h, rows, round_p, *, no_rescale=False, l_unrounded=False):
+    g = oattn.kv_head(h, q.shape[2], k.shape[2])
+    c2 = scale / np.log(2.0)
+    res = []
+    for i in rows:
+        qi = q[b, i, h].astype(np.float64)
+        m, acc, l = None, np.zeros(v.shape[3]), 0.0
+        for j in range(i // 128 + 1):
+            k0, k1 = 128 * j, min(128 * j + 128, i + 1)
+            x = (k[b, k0:k1, g].astype(np.float64) @ qi) * c2
+            m_new = oattn.stale_max_step(m, float(np.max(x)))
+            if m is not None and m_new != m and not no_rescale:
+                acc *= 2.0 ** (m - m_new)
+                l *= 2.0 ** (m - m_new)
+            m = m_new
+            exact = np.exp2(x - m)
+            p = oattn.bf16_rne(exact) if round_p else exact
+            acc += p @ v[b, k0:k1, g].astype(np.float64)
+            l += float(np.sum(exact if l_unrounded else p))
+        res.append(acc / l)
+    return np.stack(res)
+
+
+def test_bf16_mutant_without_rescale_is_caught():
+    w = CASES[2]                                   # activation-like: the maximum moves
+    q, k, v = (f32(t) for t in workloads.make_qkv(w))
+    rows = list(range(5, w.S, 23))
+    worst = max(oattn.rel_l2(_bf16_mutant(q, k, v, w.softmax_scale, 0, h, rows, False, no_rescale=True),
+                             oattn.causal_attention_rows(q, k, v, w.softmax_scale, 0, h, rows))
+                for h in range(w.Hq))
+    assert worst > 1e-6
+
+
+def test_bf16_mutant_unrounded_sum_is_caught_by_the_exact_average():
+    w = CASES[0]
+    q, k, _ = (f32(t) for t in workloads.make_qkv(w))
+    v = np.full((1, w.S, 1, 128), 0.6875)
+    bad = _bf16_mutant(q, k, v, w.softmax_scale, 0, 1, [5, 127, 128, w.S - 1], True, l_unrounded=True)
+    assert not np.all(bad == 0.6875)

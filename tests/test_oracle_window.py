@@ -172,3 +172,59 @@ def test_lean_window_keeps_the_exact_average():
     rows = [0, 5, 127, 128, 300, 519]
     out = oattn.causal_attention_rows_window(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, 1, rows, lean=True)
     assert np.all(out == c)
+
+
+# ---------------------------------------------------------------- mutations --
+# Plausible mistakes planted in a local copy of the emulation's tile loop; a
+# pin above must catch each of them.
+
+def _window_mutant(q8, qs, k8, ks, v8, vs, scale, b, h, rows, round_p, *, no_rescale=False,
+                   l_without_sv=False, no_lsv=False, l_unrounded=False):
+    g = oattn.kv_head(h, q8.shape[2], k8.shape[2])
+    c2 = scale / math.log(2.0)
+    res = []
+    for i in rows:
+        qc = ofp8.e4m3_decode(q8[b, i, h])
+        sq = float(qs[b, h, i // 128])
+        o = top = None
+        acc, l = np.zeros(v8.shape[3]), 0.0
+        for j in range(i // 128 + 1):
+            k0, k1 = 128 * j, min(128 * j + 128, i + 1)
+            kc, vc = ofp8.e4m3_decode(k8[b, k0:k1, g]), ofp8.e4m3_decode(v8[b, k0:k1, g])
+            sk, sv = float(ks[b, g, j]), float(vs[b, g, j])
+            x = (kc @ qc) * (sq * sk * c2)
+            lsv = 0.0 if no_lsv else math.log2(sv)
+            o_new, top = oattn.window_step(o, top, float(np.max(x)) + lsv)
+            if o is not None and o_new != o and not no_rescale:
+                acc *= 2.0 ** (o - o_new)
+                l *= 2.0 ** (o - o_new)
+            o = o_new
+            exact = np.exp2(x + lsv - o)
+            p = ofp8.e4m3_decode(ofp8.e4m3_rne(exact)) if round_p else exact
+            acc += p @ vc
+            l += float(np.sum(exact if l_unrounded else p)) / (1.0 if l_without_sv else sv)
+        res.append(acc / l)
+    return np.stack(res)
+
+
+@pytest.mark.parametrize("flag", ["no_rescale", "l_without_sv", "no_lsv"])
+def test_window_mutants_are_caught_by_exact_attention(flag):
+    w = CASES[2]                                   # activation-like: offsets move both ways
+    (cq, sq), (ck, sk), (cv, sv) = _quantised(w)
+    dq, dk, dv = (ofp8.dequantize_fp8(c, s) for c, s in ((cq, sq), (ck, sk), (cv, sv)))
+    rows = list(range(5, w.S, 23))
+    worst = 0.0
+    for h in range(w.Hq):
+        bad = _window_mutant(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, h, rows, False, **{flag: True})
+        ex = oattn.causal_attention_rows(dq, dk, dv, w.softmax_scale, 0, h, rows)
+        worst = max(worst, oattn.rel_l2(bad, ex))
+    assert worst > 1e-6
+
+
+def test_window_mutant_unrounded_sum_is_caught_by_the_exact_average():
+    w = workloads.custom(1, 2, 1, 520, seed=24)
+    (cq, sq), (ck, sk), _ = _quantised(w)
+    c = 448.0 * 2.0 ** -5
+    cv, sv = ofp8.quantize_fp8(np.full((1, w.S, 1, 128), c, dtype=np.float32))
+    bad = _window_mutant(cq, sq, ck, sk, cv, sv, w.softmax_scale, 0, 1, [5, 127, 300, 519], True, l_unrounded=True)
+    assert not np.all(bad == c)
